@@ -1,0 +1,413 @@
+#!/usr/bin/env python3
+"""Benchmark of the prefill MoE expert layer (routing + 4-bit grouped GEMM).
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+                    [--workload t4096] [--block-m 128]
+
+One step = one full MoE layer call (routing, gate/up pass, down pass, bf16
+finalize) over one batch of T tokens of synthetic input already resident in
+HBM. Steps cycle through independent layer sets (weights, x, logits) whose
+weights alone exceed the 129 MB L2. Prints ONE JSON line on rank 0.
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+layer is independent per token batch: weak scaling, no data-path collective);
+the time is the max over ranks.
+
+--impl reference times the CPU oracle (plain numpy, float64) on a bounded
+sample of the same workload on the host cores.
+"""
+import os
+
+# The CPU baseline is the oracle as it stands, single-threaded; fix the BLAS
+# thread count before numpy loads so that "cores" is what it really used.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer prefill tokens/s at T=4096; grouped-GEMM % of GB300 BF16 TC peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["route_select_scan", "route_scatter", "gemm_gate_up_swiglu", "gemm_down_combine",
+          "finalize_bf16"]
+KERNEL_SOURCES = ["gemm.cu", "dequant.cuh", "ptx.cuh"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="t4096")
+    p.add_argument("--block-m", type=int, default=128)
+    p.add_argument("--sets", type=int, default=2, help="independent layer sets cycled per step")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "routing_q4_grouped_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
+    if that summary was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"gemm_gate_up_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    hm = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    if not m or not hm or hm.group(1) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample(cfg, n_groups, first_group, block_m):
+    """Times the oracle on a bounded sample of one layer and scales it to the
+    whole layer by rows: routing of all T tokens, then the FFN of `n_groups`
+    consecutive routed expert groups. Returns (seconds for the full layer, note)."""
+    import oracle as O
+    from routing_q4_grouped_gb300 import synth
+
+    T = cfg.tokens_per_call
+    W = synth.gen_weights(cfg, 0)
+    x = synth.gen_x(cfg, T)
+    logits = synth.gen_logits(cfg, 0, T)
+    t0 = time.perf_counter()
+    r = O.route(logits, cfg.k, block_m)
+    t_route = time.perf_counter() - t0
+    groups = [(first_group + i) % cfg.E for i in range(n_groups)]
+    groups = [g for g in groups if r.counts[g] > 0] or [int(np.argmax(r.counts))]
+    rows = int(sum(r.counts[g] for g in groups))
+    t0 = time.perf_counter()
+    O.expert_ffn(x, W, r, experts=groups, shared=False)
+    t_ffn = time.perf_counter() - t0
+    total_rows = T * cfg.k + (T if cfg.f_s else 0)
+    full = t_route + t_ffn * total_rows / rows
+    note = (f"routing of all {T} tokens + FFN of {len(groups)} expert groups ({rows} of "
+            f"{total_rows} rows incl. shared), scaled by rows to one full layer")
+    return full, note
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from routing_q4_grouped_gb300 import synth
+
+    cfg = synth.CONFIGS[args.workload]
+    T = cfg.tokens_per_call
+    for i in range(args.warmup):
+        oracle_sample(cfg, 2, 7 * i, args.block_m)
+    times, note = [], ""
+    for i in range(args.steps):
+        t, note = oracle_sample(cfg, 2, 11 * i + 3, args.block_m)
+        times.append(t)
+    sec = statistics.mean(times)
+    value = T / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator, same recipe as the GPU arm)",
+        "config": {"workload": args.workload, "T": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+                   "f": cfg.f, "f_s": cfg.f_s, "block_m": args.block_m},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "per step: " + note},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- GPU arm
+
+
+def run_ours(args):
+    import torch
+
+    from routing_q4_grouped_gb300 import moeq4, synth
+
+    world, rank, local = dist_setup()
+    cfg = synth.CONFIGS[args.workload]
+    T, d, E, k, f, fs = cfg.tokens_per_call, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_s
+    stream = torch.cuda.current_stream()
+
+    # independent layer sets (weights, x, logits); rank r draws layers r*S .. r*S+S-1
+    sets = []
+    for i in range(args.sets):
+        layer = rank * args.sets + i
+        W = moeq4.DeviceWeights.from_host(synth.gen_weights(cfg, layer))
+        x_h = synth.gen_x(cfg, T, layer)
+        l_h = synth.gen_logits(cfg, layer, T)
+        x = torch.from_numpy(x_h.view(np.int16)).cuda().view(torch.bfloat16)
+        lg = torch.from_numpy(l_h).cuda()
+        sets.append((W, x, lg, x_h, l_h))
+    route = moeq4.RouteBuffers.alloc(T, E, k, args.block_m)
+    ws = moeq4.alloc_workspace(moeq4.moe_layer_workspace_size(T, E, k, d, f, fs))
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    weight_bytes = sets[0][0].nbytes
+
+    def step(i):
+        W, x, lg = sets[i % len(sets)][:3]
+        moeq4.moe_layer(x, lg, W, route, y, ws, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if moeq4.moe_get_device_error(route) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region: K steps, inputs resident in HBM
+    clocks = ClockSampler(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
+    ms_step = ms_total / args.steps
+    value = T * world * args.steps / (ms_total * 1e-3)
+    launches = 5 * args.steps
+
+    # ---- per-kernel times over the same K steps, stage events on the launching stream
+    stage_ms = {s: [] for s in STAGES}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        moeq4.moe_debug_set_stage_events(evs[i])
+        step(i)
+    moeq4.moe_debug_set_stage_events([])
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        for j, s in enumerate(STAGES):
+            stage_ms[s].append(evs[i][j].elapsed_time(evs[i][j + 1]))
+    kern = {s: statistics.mean(v) for s, v in stage_ms.items()}
+
+    # ---- end to end through the public call: pinned H2D of x + logits, layer, D2H of y
+    pins = [(torch.from_numpy(s[3].view(np.int16)).pin_memory(),
+             torch.from_numpy(s[4]).pin_memory()) for s in sets]
+    x_dev = torch.empty_like(sets[0][1])
+    l_dev = torch.empty_like(sets[0][2])
+    y_host = torch.empty((T, d), dtype=torch.int16).pin_memory()
+
+    def e2e_step(i):
+        xh, lh = pins[i % len(pins)]
+        x_dev.view(torch.int16).copy_(xh, non_blocking=True)
+        l_dev.copy_(lh, non_blocking=True)
+        moeq4.moe_layer(x_dev, l_dev, sets[i % len(sets)][0], route, y, ws, stream)
+        y_host.copy_(y.view(torch.int16), non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, ev0.elapsed_time(ev1))
+    e2e_value = T * world * args.steps / (e2e_ms * 1e-3)
+    h2d = T * d * 2 + T * E * 4
+    d2h = T * d * 2
+
+    if moeq4.moe_get_device_error(route) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # ---- roofline of the dominant kernel (the gate/up pass) and of the grouped GEMM
+    pk, pk_src = peaks()
+    flops_gu = 4 * d * f * T * k + 4 * d * fs * T
+    flops_dn = 2 * d * f * T * k + 2 * d * fs * T
+    counts = route.counts.cpu().numpy()
+    touched = int((counts > 0).sum())
+    per_expert_gu = 2 * f * d // 2 + 2 * f * (d // 64) * 4
+    per_expert_dn = d * f // 2 + d * (f // 64) * 4
+    sh_gu = 2 * fs * d // 2 + 2 * fs * (d // 64) * 4
+    sh_dn = d * fs // 2 + d * (fs // 64) * 4
+    bytes_gu = touched * per_expert_gu + sh_gu + T * d * 2 + T * k * f * 2 + T * fs * 2
+    peak_tf = pk["bf16_tflops"]
+    peak_gb = pk["hbm_gbs"]
+    t_gu = kern["gemm_gate_up_swiglu"] * 1e-3
+    t_dn = kern["gemm_down_combine"] * 1e-3
+    tensor_time = flops_gu / (peak_tf * 1e12)
+    hbm_time = bytes_gu / (peak_gb * 1e9)
+    if tensor_time >= hbm_time:
+        roof = {"bound": "tensor", "achieved": flops_gu / t_gu / 1e12, "peak": peak_tf,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": bytes_gu / t_gu / 1e9, "peak": peak_gb, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic(args.workload)
+    roof["kernel"] = "q4_grouped_gemm_kernel<0> (gate/up + SwiGLU)"
+    roof["peak_source"] = f"{pk_src} (bf16 burst / hbm copy)"
+    gg_tflops = (flops_gu + flops_dn) / (t_gu + t_dn) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init 4-bit weights)",
+        "config": {"workload": args.workload, "T": T, "d": d, "E": E, "k": k, "f": f, "f_s": fs,
+                   "block_m": args.block_m, "layer_sets": args.sets,
+                   "l2": f"inputs larger than L2: {args.sets} layer sets of "
+                         f"{weight_bytes / 1e6:.0f} MB weights cycled per step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "grouped_gemm": {"tflops": gg_tflops, "frac_bf16_peak": gg_tflops / peak_tf,
+                         "ms": (t_gu + t_dn) * 1e3},
+        "kernels_ms": kern,
+        "touched_experts": touched,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_full, note = oracle_sample(cfg, 4, 0, args.block_m)
+        line["cpu_baseline"] = {"value": T / t_full, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": note}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,47 @@
+/*
+ * moeq4_debug.h — test-only entry points of libmoeq4. They expose single
+ * building blocks of the expert-layer kernels so that each can be checked on
+ * its own; none is on the hot path and none is needed to run the layer.
+ * Same conventions as moeq4.h (device pointers, asynchronous on `stream`,
+ * negative status on bad arguments).
+ */
+#ifndef MOEQ4_DEBUG_H
+#define MOEQ4_DEBUG_H
+
+#include <stdint.h>
+
+#include "moeq4.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Expands a 4-bit groupwise-affine matrix to bf16 in global memory with the
+ * same register routine the grouped GEMM uses ("Perplexity Lily 오픈소스 공개 …",
+ * §5-1 format; value bf16(scale*q + bias) rounded once).
+ *   qw [rows][K/8] uint32, scale/bias [rows][K/64] bf16  ->  out [rows][K] bf16.
+ * K % 64 == 0. The product path never materialises this array. */
+moe_status moe_debug_dequant(const uint32_t* qw, const uint16_t* scale, const uint16_t* bias,
+                             int32_t rows, int32_t K, uint16_t* out, void* stream);
+
+/* One CTA computes D[128][N] = A[128][K] * B[N][K]^T (bf16 in, fp32 out, all
+ * row-major) with tcgen05.mma: B is staged in shared memory in the 128-byte
+ * swizzled K-major layout; A is staged the same way (a_from_tmem = 0) or
+ * written to tensor memory with tcgen05.st (a_from_tmem = 1). K % 64 == 0,
+ * 64 <= K <= 1024, N % 16 == 0, 16 <= N <= 256. */
+moe_status moe_debug_mma(int32_t a_from_tmem, const uint16_t* A, const uint16_t* B, float* D,
+                         int32_t N, int32_t K, void* stream);
+
+/* Stage timing for benchmarks: with n > 0, moe_route / moe_expert_ffn /
+ * moe_layer record events[i] (cudaEvent_t handles created by the caller) on
+ * the call's stream at stage boundaries: 0 before routing, 1 after selection +
+ * lookback scan, 2 after the scatter, 3 after the gate/up pass, 4 after the
+ * down pass, 5 after the bf16 finalize. n = 0 turns it off. Process-wide;
+ * not for concurrent use from several threads. */
+moe_status moe_debug_set_stage_events(void* const* events, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEQ4_DEBUG_H */

@@ -225,7 +225,7 @@ def _ffn_one(X, qgu, sgu, bgu, qdn, sdn, bdn, f):
     return A @ Wd.T
 
 
-def expert_ffn(x_bits, W, r: Route, tokens=None, return_acc=False):
+def expert_ffn(x_bits, W, r: Route, tokens=None, return_acc=False, experts=None, shared=True):
     """Grouped expert FFN with weighted combine and the shared expert.
 
     For each expert e and each row of its group (token t, slot j):
@@ -235,7 +235,9 @@ def expert_ffn(x_bits, W, r: Route, tokens=None, return_acc=False):
     are expanded per expert with :func:`dequant` ([A] §5-1).
 
     ``tokens``: optional sorted token subset; rows of other tokens are skipped
-    (the layer is independent per token). Returns bf16 bits [len(tokens) or T, d].
+    (the layer is independent per token). ``experts`` / ``shared``: restrict the
+    work to some expert groups (used to time a bounded sample of the layer).
+    Returns bf16 bits [len(tokens) or T, d].
     """
     x_bits = np.asarray(x_bits)
     T, d = x_bits.shape
@@ -245,7 +247,7 @@ def expert_ffn(x_bits, W, r: Route, tokens=None, return_acc=False):
     where[tok_list] = np.arange(len(tok_list))
     acc = np.zeros((len(tok_list), d), dtype=np.float64)
     X = bf16_value(x_bits)
-    for e in range(E):
+    for e in (range(E) if experts is None else experts):
         rows = r.perm[r.offsets[e]:r.offsets[e + 1]].astype(np.int64)
         t, j = rows // k, rows % k
         keep = where[t] >= 0
@@ -255,7 +257,7 @@ def expert_ffn(x_bits, W, r: Route, tokens=None, return_acc=False):
         out = _ffn_one(X[t], W.gu_qw[e], W.gu_scale[e], W.gu_bias[e],
                        W.dn_qw[e], W.dn_scale[e], W.dn_bias[e], W.f)
         acc[where[t]] += r.w[t, j].astype(np.float64)[:, None] * out
-    if W.f_s:
+    if W.f_s and shared:
         out = _ffn_one(X[tok_list], W.sgu_qw[0], W.sgu_scale[0], W.sgu_bias[0],
                        W.sdn_qw[0], W.sdn_scale[0], W.sdn_bias[0], W.f_s)
         acc += out

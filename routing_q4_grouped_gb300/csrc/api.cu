@@ -1,0 +1,372 @@
+// api.cu — the extern "C" boundary of libmoeq4: argument validation,
+// workspace layout, TMA descriptor encoding and the launch sequence.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moeq4.h"
+#include "../../include/moeq4_debug.h"
+#include "internal.h"
+
+namespace moeq4 {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base,
+               uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * esize};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+  int sms = 0;
+  bool sm103 = false;
+};
+
+// Per-device constants, looked up once per device.
+moe_status device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> g(mu);
+  if (!have[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    cache[dev].sms = sms;
+    cache[dev].sm103 = (major == 10 && minor == 3);
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  return out->sm103 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+uint64_t timeout_ns() {
+  static uint64_t t = [] {
+    const char* s = std::getenv("MOEQ4_WAIT_TIMEOUT_MS");
+    long ms = s ? std::atol(s) : 2000;
+    if (ms <= 0) ms = 2000;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return t;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_route_out(const moe_route_out* r) {
+  if (!r) return MOE_ERR_ARG;
+  if (r->T < 0 || r->E < 1 || r->E > 1024 || r->k < 1 || r->k > r->E || r->k > 32 ||
+      r->block_m < 1 || r->block_m > 128)
+    return MOE_ERR_ARG;
+  if (static_cast<long long>(r->T) * r->k >= (1ll << 30)) return MOE_ERR_SHAPE;
+  const void* always[] = {r->counts, r->offsets, r->tiles, r->n_tiles, r->err};
+  const void* per_token[] = {r->ids, r->w, r->perm, r->inv};   // may be NULL when T == 0
+  for (const void* p : always) {
+    if (!p) return MOE_ERR_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  }
+  for (const void* p : per_token) {
+    if (!p && r->T > 0) return MOE_ERR_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  }
+  return MOE_OK;
+}
+
+moe_status check_mat(const moe_q4_mat& m) {
+  if (!m.qw || !m.scale || !m.bias) return MOE_ERR_ARG;
+  if (!aligned16(m.qw) || !aligned16(m.scale) || !aligned16(m.bias)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+moe_status check_weights(const moe_q4_weights* W) {
+  if (!W) return MOE_ERR_ARG;
+  if (W->E < 1 || W->E > 1024 || W->d < 1 || W->f < 1 || W->f_s < 0) return MOE_ERR_ARG;
+  if (W->d % 128 || W->f % 128 || W->f_s % 128 || W->d > 16384 || W->f > 8192 || W->f_s > 8192)
+    return MOE_ERR_SHAPE;
+  moe_status s;
+  if ((s = check_mat(W->gate_up)) != MOE_OK || (s = check_mat(W->down)) != MOE_OK) return s;
+  if (W->f_s > 0 &&
+      ((s = check_mat(W->sh_gate_up)) != MOE_OK || (s = check_mat(W->sh_down)) != MOE_OK))
+    return s;
+  return MOE_OK;
+}
+
+RouteArgs make_route_args(const float* logits, const moe_route_out* r, void* ws) {
+  RouteArgs a{};
+  const RouteWs L = route_ws_layout(r->T, r->E, r->k);
+  char* base = static_cast<char*>(ws);
+  a.logits = logits;
+  a.T = r->T;
+  a.E = r->E;
+  a.k = r->k;
+  a.block_m = r->block_m;
+  a.nblk = r->T > 0 ? (r->T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock : 1;
+  a.ids = r->ids;
+  a.w = r->w;
+  a.counts = r->counts;
+  a.offsets = r->offsets;
+  a.perm = r->perm;
+  a.inv = r->inv;
+  a.tiles = r->tiles;
+  a.n_tiles = r->n_tiles;
+  a.err = r->err;
+  a.lb = reinterpret_cast<uint32_t*>(base + L.lb);
+  a.blk_base = reinterpret_cast<int32_t*>(base + L.blk_base);
+  a.lrank = reinterpret_cast<int32_t*>(base + L.lrank);
+  a.ctr = reinterpret_cast<int32_t*>(base + L.ctr);
+  a.timeout_ns = timeout_ns();
+  return a;
+}
+
+moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, size_t ws_bytes,
+                      cudaStream_t s) {
+  moe_status st = check_route_out(r);
+  if (st != MOE_OK) return st;
+  if ((!logits && r->T > 0) || !ws) return MOE_ERR_ARG;
+  if (!aligned16(logits) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  if (ws_bytes < route_ws_layout(r->T, r->E, r->k).total) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const RouteArgs a = make_route_args(logits, r, ws);
+  stage_mark(0, s);
+  if (launch_route_select(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  stage_mark(1, s);
+  if (launch_route_scatter(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  stage_mark(2, s);
+  return MOE_OK;
+}
+
+moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weights* W,
+                    const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
+                    cudaStream_t s) {
+  moe_status st = check_route_out(r);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(W)) != MOE_OK) return st;
+  if (!x || !y || !ws) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  if (T != r->T || d != W->d || W->E != r->E) return MOE_ERR_SHAPE;
+  const int k = r->k, E = W->E, f = W->f, fs = W->f_s;
+  const FfnWs L = ffn_ws_layout(T, k, d, f, fs);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+
+  char* base = static_cast<char*>(ws);
+  GemmArgs a{};
+  a.E = E;
+  a.T = T;
+  a.k = k;
+  a.d = d;
+  a.f = f;
+  a.f_s = fs;
+  a.tiles = r->tiles;
+  a.n_tiles = r->n_tiles;
+  a.max_tiles = moe_route_max_tiles(T, E, k, r->block_m);
+  a.perm = r->perm;
+  a.wts = r->w;
+  a.act = reinterpret_cast<uint16_t*>(base + L.act);
+  a.act_sh = reinterpret_cast<uint16_t*>(base + L.act_sh);
+  a.y_acc = reinterpret_cast<float*>(base + L.y_acc);
+  a.err = r->err;
+  a.timeout_ns = timeout_ns();
+
+  CUtensorMap tmA, tmA_sh, tmB, tmB_sh;
+  const CUtensorMapSwizzle SW32 = CU_TENSOR_MAP_SWIZZLE_32B, SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+  const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+  // ---- pass 0: gate/up + SwiGLU
+  {
+    GemmArgs g = a;
+    g.K = d;
+    g.K_sh = d;
+    g.n_fb = f / 128;
+    g.n_fb_sh = fs / 128;
+    g.n_sh_tiles = fs ? (T + gemm_tile_rows(0) - 1) / gemm_tile_rows(0) : 0;
+    g.scale = W->gate_up.scale;
+    g.bias = W->gate_up.bias;
+    g.sh_scale = fs ? W->sh_gate_up.scale : W->gate_up.scale;
+    g.sh_bias = fs ? W->sh_gate_up.bias : W->gate_up.bias;
+    bool ok = encode_2d(&tmA, U32, 4, W->gate_up.qw, d / 8, static_cast<uint64_t>(E) * 2 * f, 8,
+                        128, SW32) &&
+              encode_2d(&tmB, BF16, 2, x, d, T, 64, 1, SW128);
+    if (fs) ok = ok && encode_2d(&tmA_sh, U32, 4, W->sh_gate_up.qw, d / 8, 2ull * fs, 8, 128, SW32);
+    else tmA_sh = tmA;
+    tmB_sh = tmB;
+    if (!ok) return MOE_ERR_CUDA;
+    if (launch_gemm(0, g, tmA, tmA_sh, tmB, tmB_sh, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    stage_mark(3, s);
+  }
+  // ---- pass 1: down + weighted combine (+ shared expert)
+  {
+    GemmArgs g = a;
+    g.K = f;
+    g.K_sh = fs;
+    g.n_fb = d / 128;
+    g.n_fb_sh = fs ? d / 128 : 0;
+    g.n_sh_tiles = fs ? (T + gemm_tile_rows(1) - 1) / gemm_tile_rows(1) : 0;
+    g.scale = W->down.scale;
+    g.bias = W->down.bias;
+    g.sh_scale = fs ? W->sh_down.scale : W->down.scale;
+    g.sh_bias = fs ? W->sh_down.bias : W->down.bias;
+    bool ok = encode_2d(&tmA, U32, 4, W->down.qw, f / 8, static_cast<uint64_t>(E) * d, 8, 128,
+                        SW32) &&
+              encode_2d(&tmB, BF16, 2, a.act, f, static_cast<uint64_t>(T) * k, 64, 16, SW128);
+    if (fs)
+      ok = ok && encode_2d(&tmA_sh, U32, 4, W->sh_down.qw, fs / 8, d, 8, 128, SW32) &&
+           encode_2d(&tmB_sh, BF16, 2, a.act_sh, fs, T, 64, 16, SW128);
+    else {
+      tmA_sh = tmA;
+      tmB_sh = tmB;
+    }
+    if (!ok) return MOE_ERR_CUDA;
+    if (launch_gemm(1, g, tmA, tmA_sh, tmB, tmB_sh, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    stage_mark(4, s);
+  }
+  if (launch_finalize(a.y_acc, y, static_cast<size_t>(T) * d, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  stage_mark(5, s);
+  return MOE_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+std::mutex g_ev_mu;
+cudaEvent_t g_events[8] = {};
+int g_nevents = 0;
+
+}  // namespace
+
+void stage_mark(int i, cudaStream_t s) {
+  if (g_nevents == 0) return;   // the common case: no timing requested
+  std::lock_guard<std::mutex> g(g_ev_mu);
+  if (i < g_nevents && g_events[i]) cudaEventRecord(g_events[i], s);
+}
+
+}  // namespace moeq4
+
+using namespace moeq4;
+
+extern "C" {
+
+int32_t moe_route_max_tiles(int32_t T, int32_t E, int32_t k, int32_t block_m) {
+  if (T < 0 || E < 1 || k < 1 || block_m < 1) return 0;
+  const long long rows = static_cast<long long>(T) * k;
+  const long long n = rows / block_m + (rows < E ? rows : E);
+  return static_cast<int32_t>(n);
+}
+
+size_t moe_route_workspace_size(int32_t T, int32_t E, int32_t k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  return route_ws_layout(T, E, k).total;
+}
+
+size_t moe_ffn_workspace_size(int32_t T, int32_t k, int32_t d, int32_t f, int32_t f_s) {
+  if (T < 0 || k < 1 || d < 1 || f < 1 || f_s < 0) return 0;
+  return ffn_ws_layout(T, k, d, f, f_s).total;
+}
+
+size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
+                                int32_t f_s) {
+  const size_t a = moe_route_workspace_size(T, E, k), b = moe_ffn_workspace_size(T, k, d, f, f_s);
+  if (!a || !b) return 0;
+  return align256(a) + b;
+}
+
+moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, size_t ws_bytes,
+                     void* stream) {
+  return route_impl(logits, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weights* W,
+                          const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
+                          void* stream) {
+  return ffn_impl(x, T, d, W, r, y, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_weights* W,
+                     const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (!W || !r) return MOE_ERR_ARG;
+  if (r->T != T) return MOE_ERR_SHAPE;
+  const size_t need = moe_layer_workspace_size(T, r->E, r->k, W->d, W->f, W->f_s);
+  if (!ws || need == 0 || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  const size_t rsz = align256(moe_route_workspace_size(T, r->E, r->k));
+  moe_status st;
+  // validate the FFN arguments before anything is enqueued
+  if ((st = check_weights(W)) != MOE_OK) return st;
+  if (!x || !y) return MOE_ERR_ARG;
+  if (W->E != r->E) return MOE_ERR_SHAPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = route_impl(logits, r, ws, rsz, s)) != MOE_OK) return st;
+  return ffn_impl(x, T, W->d, W, r, y, static_cast<char*>(ws) + rsz, ws_bytes - rsz, s);
+}
+
+moe_status moe_get_device_error(const int32_t* err, int32_t* code, void* stream) {
+  if (!err || !code) return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *code = v;
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status moe_debug_set_stage_events(void* const* events, int32_t n) {
+  if (n < 0 || n > 8 || (n > 0 && !events)) return MOE_ERR_ARG;
+  std::lock_guard<std::mutex> g(g_ev_mu);
+  for (int i = 0; i < 8; ++i) g_events[i] = (i < n) ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  g_nevents = n;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case MOE_ERR_DEVICE: return "device error word is set";
+    case MOE_ERR_UNSUPPORTED: return "device is not sm_103";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

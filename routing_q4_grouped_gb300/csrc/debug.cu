@@ -1,0 +1,148 @@
+// debug.cu — test-only entry points (moeq4_debug.h): the dequantisation routine
+// writing to global memory, and a single-CTA tcgen05 MMA over operands staged
+// by plain threads. They isolate the building blocks of the grouped GEMM.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moeq4_debug.h"
+#include "dequant.cuh"
+#include "ptx.cuh"
+
+namespace moeq4 {
+namespace {
+
+__global__ void __launch_bounds__(256) dequant_probe_kernel(const uint32_t* __restrict__ qw,
+                                                            const uint16_t* __restrict__ scale,
+                                                            const uint16_t* __restrict__ bias,
+                                                            int rows, int K, uint16_t* out) {
+  const size_t wpr = static_cast<size_t>(K) / 8;
+  const size_t n = static_cast<size_t>(rows) * wpr;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n; i += stride) {
+    const size_t row = i / wpr, w = i % wpr;
+    const size_t g = row * (K / 64) + w / 8;
+    uint32_t v[4];
+    dequant8(qw[i], bf16_pair(scale[g]), bf16_pair(bias[g]), v);
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+// Stages rows [0, nrows) x K-chunk c of M (row-major, K columns) in the
+// 128-byte swizzled K-major layout: 16-byte piece j of row r at r*128 + (j ^ (r%8))*16.
+__device__ void stage_sw128(uint8_t* dst, const uint16_t* M, int nrows, int K, int c) {
+  for (int i = threadIdx.x; i < nrows * 8; i += blockDim.x) {
+    const int r = i >> 3, j = i & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(M + static_cast<size_t>(r) * K + c * 64 + j * 8);
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ (r & 7)) * 16)) = v;
+  }
+}
+
+__global__ void __launch_bounds__(128, 1) mma_probe_kernel(int a_tmem, const uint16_t* A,
+                                                           const uint16_t* B, float* D, int N,
+                                                           int K, int32_t* status) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = sm;            // 128 x 128 B
+  uint8_t* sB = sm + 16384;    // N x 128 B
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  __shared__ int zero;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    zero = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tbase, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tbase;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t idesc = idesc_bf16_f32(128, N);
+  bool ok = true;
+  for (int c = 0; c < K / 64 && ok; ++c) {
+    stage_sw128(sB, B, N, K, c);
+    if (!a_tmem) {
+      stage_sw128(sA, A, 128, K, c);
+    } else {
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(A + static_cast<size_t>(tid) * K + c * 64);
+      uint32_t v[16];
+      for (int i = 0; i < 16; ++i) v[i] = row[i];
+      tmem_st_32x32b_x16(tmem + lane_base, v);
+      for (int i = 0; i < 16; ++i) v[i] = row[16 + i];
+      tmem_st_32x32b_x16(tmem + lane_base + 16, v);
+      tmem_st_wait();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bd = sdesc_k_sw128(smem_u32(sB) + kk * 32);
+        if (a_tmem) mma_ts(tmem + 256, tmem + kk * 8, bd, idesc, (c | kk) != 0);
+        else mma_ss(tmem + 256, sdesc_k_sw128(smem_u32(sA) + kk * 32), bd, idesc, (c | kk) != 0);
+      }
+      mma_commit(&bar);
+    }
+    ok = mbar_wait(&bar, c & 1, &zero, 1000000000ull);
+    tc_fence_after();
+    __syncthreads();
+  }
+  if (!ok) {
+    if (tid == 0 && status) *status = 1;
+  } else {
+    for (int cc = 0; cc * 32 < N; ++cc) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tmem + lane_base + 256 + cc * 32, v);
+      tmem_ld_wait();
+      for (int j = 0; j < 32; ++j)
+        if (cc * 32 + j < N) D[static_cast<size_t>(tid) * N + cc * 32 + j] = __uint_as_float(v[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+}  // namespace moeq4
+
+using namespace moeq4;
+
+extern "C" moe_status moe_debug_dequant(const uint32_t* qw, const uint16_t* scale,
+                                        const uint16_t* bias, int32_t rows, int32_t K,
+                                        uint16_t* out, void* stream) {
+  if (!qw || !scale || !bias || !out || rows < 0 || K <= 0 || K % 64) return MOE_ERR_ARG;
+  if (rows == 0) return MOE_OK;
+  const size_t n = static_cast<size_t>(rows) * (K / 8);
+  const int grid = static_cast<int>(n / 256 + 1 < 8192 ? n / 256 + 1 : 8192);
+  dequant_probe_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(qw, scale, bias, rows,
+                                                                            K, out);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status moe_debug_mma(int32_t a_from_tmem, const uint16_t* A, const uint16_t* B,
+                                    float* D, int32_t N, int32_t K, void* stream) {
+  if (!A || !B || !D || N < 16 || N > 256 || N % 16 || K < 64 || K > 1024 || K % 64)
+    return MOE_ERR_ARG;
+  const size_t smem = 1024 + 16384 + 256 * 128;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr = true;
+  }
+  // a wait that gives up leaves D unwritten, which the caller's comparison catches
+  mma_probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(a_from_tmem, A, B, D, N,
+                                                                        K, nullptr);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,318 @@
+// route.cu — GPU routing for the MoE expert layer: per-token top-k expert
+// selection with renormalised softmax weights, a deterministic per-block
+// histogram with stable local ranks, a single-pass decoupled-lookback prefix
+// over blocks, offsets + block map by the last block to finish, then the
+// scatter. Two kernels on one stream, no host synchronisation.
+//
+// Step order: "Apple silicon용 Lily, Qwen 추론 최적화" (aitrends.kr), section
+// "GPU 상주와 메모리 절감" — per-token expert selection, a histogram of
+// allocations, a prefix scan for start offsets, a scatter of rows into expert
+// groups, all kept on the GPU; "Perplexity Lily 오픈소스 공개 …" (alltoptrend.co.kr),
+// §5-2 — histogram, prefix scan, scatter and block map in one GPU command buffer.
+#include <cmath>
+#include <climits>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "../../include/moeq4.h"
+
+namespace moeq4 {
+
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// (v1, e1) ranks before (v2, e2): larger logit first, equal logits by lower index.
+__device__ __forceinline__ bool ranks_before(float v1, int e1, float v2, int e2) {
+  return v1 > v2 || (v1 == v2 && e1 < e2);
+}
+
+// Kernel 1: selection, histogram with stable local ranks, lookback prefix,
+// and (in the last block to finish) counts, offsets and the block map.
+// S = logits held per lane (E <= 32 * S). One warp handles one token at a time.
+template <int S>
+__global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const RouteArgs a) {
+  extern __shared__ int smem[];
+  __shared__ int s_b, s_last;
+  __shared__ int s_wsum[2][kRouteThreads / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, k = a.k;
+  int* sE = smem;                                   // [TB * k] expert of each block row
+  int* sCnt = sE + kRouteTokensPerBlock * k;        // [E]     running per-expert counts
+  int* sLead = sCnt + E;                            // [256]   group base handed to peers
+
+  if (tid == 0) s_b = atomicAdd(&a.ctr[0], 1);      // virtual block id = arrival order
+  for (int e = tid; e < E; e += kRouteThreads) sCnt[e] = 0;
+  __syncthreads();
+  const int b = s_b;
+  if (b >= a.nblk) {   // the counters were not zero at launch: refuse to write out of range
+    if (tid == 0) atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);
+    return;
+  }
+  const int t0 = b * kRouteTokensPerBlock;
+  const int nt = max(0, min(kRouteTokensPerBlock, a.T - t0));
+
+  // ---- per-token top-k on the fp32 logits + weights
+  for (int i = warp; i < nt; i += kRouteThreads / 32) {
+    const int t = t0 + i;
+    const float* row = a.logits + static_cast<size_t>(t) * E;
+    float v[S];
+    bool bad = false;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      const int e = lane + 32 * s;
+      float x = -INFINITY;
+      if (e < E) {
+        x = __ldg(row + e);
+        if (!isfinite(x)) {
+          bad = true;
+          if (isnan(x)) x = -INFINITY;
+        }
+      }
+      v[s] = x;
+    }
+    if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
+
+    uint32_t used = 0;
+    int my_e = 0;
+    float my_v = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = INT_MAX;
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        const int e = lane + 32 * s;
+        if (e < E && !((used >> s) & 1u) && ranks_before(v[s], e, bv, be)) {
+          bv = v[s];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (ranks_before(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) used |= 1u << (be >> 5);
+      if (lane == j) {
+        my_e = be;
+        my_v = bv;
+      }
+    }
+    // renormalised softmax over the chosen experts: exp(l_j - l_max) / sum, in fp64
+    const float m = __shfl_sync(kFull, my_v, 0);
+    double ex = (lane < k) ? exp(static_cast<double>(my_v) - static_cast<double>(m)) : 0.0;
+    double sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < k) {
+      const size_t o = static_cast<size_t>(t) * k + lane;
+      a.ids[o] = my_e;
+      a.w[o] = static_cast<float>(ex / sum);
+      sE[i * k + lane] = my_e;
+    }
+  }
+  __syncthreads();
+
+  // ---- stable local ranks: rows of the block in ascending (t, j) order
+  const int n_ent = nt * k;
+  for (int base = 0; base < n_ent; base += kRouteThreads) {
+    const int i = base + tid;
+    const bool valid = i < n_ent;
+    const int e = valid ? sE[i] : -1 - lane;          // dummies never match each other
+    const uint32_t peers = __match_any_sync(kFull, e);
+    const int leader = __ffs(peers) - 1;
+    const int rk = __popc(peers & ((1u << lane) - 1u));
+    for (int w = 0; w < kRouteThreads / 32; ++w) {   // warps in order keep the ranks stable
+      if (warp == w && valid && lane == leader) {
+        const int bse = sCnt[e];
+        sCnt[e] = bse + __popc(peers);
+        sLead[w * 32 + lane] = bse;
+      }
+      __syncthreads();
+    }
+    if (valid) a.lrank[static_cast<size_t>(t0) * k + i] = sLead[warp * 32 + leader] + rk;
+    __syncthreads();
+  }
+
+  // ---- decoupled lookback over blocks, one column per expert
+  for (int e = tid; e < E; e += kRouteThreads) {
+    const uint32_t cnt = static_cast<uint32_t>(sCnt[e]);
+    uint32_t* mine = a.lb + static_cast<size_t>(b) * E + e;
+    uint32_t excl = 0;
+    if (b == 0) {
+      st_release(mine, kLbInclusive | cnt);
+    } else {
+      st_release(mine, kLbAggregate | cnt);
+      int p = b - 1;
+      uint32_t spins = 0;
+      uint64_t t_start = 0;
+      while (p >= 0) {
+        const uint32_t word = ld_acquire(a.lb + static_cast<size_t>(p) * E + e);
+        const uint32_t st = word & ~kLbValueMask;
+        if (st == 0) {
+          if ((++spins & 255u) == 0) {
+            if (t_start == 0) t_start = globaltimer_ns();
+            else if (globaltimer_ns() - t_start > a.timeout_ns) {
+              atomicOr(a.err, MOE_DEVERR_SCAN_TIMEOUT);
+              break;
+            }
+          }
+          continue;
+        }
+        excl += word & kLbValueMask;
+        if (st == kLbInclusive) break;
+        --p;
+      }
+      st_release(mine, kLbInclusive | (excl + cnt));
+    }
+    a.blk_base[static_cast<size_t>(b) * E + e] = static_cast<int32_t>(excl);
+  }
+
+  // ---- the last block to finish derives counts, offsets and the block map
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = (atomicAdd(&a.ctr[1], 1) == a.nblk - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;   // experts per thread (<= 4)
+  int c_loc[4], nt_loc[4];
+  int sc = 0, stl = 0;
+  const uint32_t* last = a.lb + static_cast<size_t>(a.nblk - 1) * E;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid * per + j;
+    int c = 0;
+    if (j < per && e < E) c = static_cast<int>(ld_acquire(last + e) & kLbValueMask);
+    c_loc[j] = c;
+    nt_loc[j] = (c + a.block_m - 1) / a.block_m;
+    sc += c;
+    stl += nt_loc[j];
+  }
+  // block-wide exclusive scan of (sc, stl)
+  int isc = sc, istl = stl;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int x = __shfl_up_sync(kFull, isc, off);
+    const int y = __shfl_up_sync(kFull, istl, off);
+    if (lane >= off) {
+      isc += x;
+      istl += y;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[0][warp] = isc;
+    s_wsum[1][warp] = istl;
+  }
+  __syncthreads();
+  int wb_c = 0, wb_t = 0, tot_c = 0, tot_t = 0;
+  for (int w = 0; w < kRouteThreads / 32; ++w) {
+    if (w < warp) {
+      wb_c += s_wsum[0][w];
+      wb_t += s_wsum[1][w];
+    }
+    tot_c += s_wsum[0][w];
+    tot_t += s_wsum[1][w];
+  }
+  int off = wb_c + isc - sc;
+  int toff = wb_t + istl - stl;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid * per + j;
+    if (j < per && e < E) {
+      a.counts[e] = c_loc[j];
+      a.offsets[e] = off;
+      for (int s = 0; s < nt_loc[j]; ++s) {
+        int32_t* tl = a.tiles + 3 * static_cast<size_t>(toff + s);
+        tl[0] = e;
+        tl[1] = off + s * a.block_m;
+        tl[2] = min(a.block_m, c_loc[j] - s * a.block_m);
+      }
+      off += c_loc[j];
+      toff += nt_loc[j];
+    }
+  }
+  if (tid == 0) {
+    a.offsets[E] = tot_c;
+    *a.n_tiles = tot_t;
+    a.ctr[0] = 0;     // ready for the next call
+    a.ctr[1] = 0;
+  }
+}
+
+// Kernel 2: scatter rows into their expert groups; clear the lookback words.
+__global__ void __launch_bounds__(256) route_scatter_kernel(const RouteArgs a) {
+  const size_t n = static_cast<size_t>(a.T) * a.k;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n; i += stride) {
+    const int e = a.ids[i];
+    const int t = static_cast<int>(i / a.k);
+    const int b = t / kRouteTokensPerBlock;
+    const int pos = a.offsets[e] + a.blk_base[static_cast<size_t>(b) * a.E + e] + a.lrank[i];
+    a.perm[pos] = static_cast<int32_t>(i);
+    a.inv[i] = pos;
+  }
+  const size_t nlb = static_cast<size_t>(a.nblk) * a.E;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < nlb; i += stride)
+    a.lb[i] = 0;
+}
+
+template <int S>
+cudaError_t launch_select(const RouteArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(int) * (kRouteTokensPerBlock * a.k + a.E + kRouteThreads);
+  route_select_kernel<S><<<a.nblk, kRouteThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+RouteWs route_ws_layout(int T, int E, int k) {
+  const int nblk = T > 0 ? (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock : 1;
+  RouteWs w{};
+  size_t o = 0;
+  w.lb = o;        o = align_up(o + sizeof(uint32_t) * nblk * E, 256);
+  w.ctr = o;       o = align_up(o + 2 * sizeof(int32_t), 256);
+  w.blk_base = o;  o = align_up(o + sizeof(int32_t) * nblk * E, 256);
+  w.lrank = o;     o = align_up(o + sizeof(int32_t) * static_cast<size_t>(T) * k, 256);
+  w.total = o;
+  return w;
+}
+
+cudaError_t launch_route_select(const RouteArgs& a, cudaStream_t s) {
+  cudaError_t err;
+  const int S = (a.E + 31) / 32;
+  if (S <= 1) err = launch_select<1>(a, s);
+  else if (S <= 2) err = launch_select<2>(a, s);
+  else if (S <= 4) err = launch_select<4>(a, s);
+  else if (S <= 8) err = launch_select<8>(a, s);
+  else if (S <= 16) err = launch_select<16>(a, s);
+  else err = launch_select<32>(a, s);
+  return err;
+}
+
+cudaError_t launch_route_scatter(const RouteArgs& a, cudaStream_t s) {
+  const size_t n = static_cast<size_t>(a.T) * a.k;
+  int grid = static_cast<int>(std::min<size_t>((n + 255) / 256 + 1, 1024));
+  route_scatter_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moeq4

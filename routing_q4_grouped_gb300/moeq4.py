@@ -1,0 +1,279 @@
+"""ctypes binding of libmoeq4 (C-ABI in include/moeq4.h), same names as the C calls.
+
+Argument marshalling only: tensors are passed as raw device pointers, the
+current CUDA stream as a handle, and every step of the layer runs in the
+library's kernels. PyTorch provides device memory and streams. There is no
+fallback: if the library is missing or the device is not sm_103 the calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoeq4.so")
+
+MOE_OK = 0
+MOE_DEVERR_NONFINITE_LOGIT = 1
+MOE_DEVERR_SCAN_TIMEOUT = 2
+MOE_DEVERR_PIPE_TIMEOUT = 4
+MOE_DEVERR_BAD_TILE = 8
+MOE_DEVERR_BAD_WORKSPACE = 16
+
+_c_i32 = ctypes.c_int32
+_c_ptr = ctypes.c_void_p
+_c_size = ctypes.c_size_t
+
+
+class Q4Mat(ctypes.Structure):
+    _fields_ = [("qw", _c_ptr), ("scale", _c_ptr), ("bias", _c_ptr)]
+
+
+class Q4WeightsC(ctypes.Structure):
+    _fields_ = [("gate_up", Q4Mat), ("down", Q4Mat), ("sh_gate_up", Q4Mat), ("sh_down", Q4Mat),
+                ("E", _c_i32), ("d", _c_i32), ("f", _c_i32), ("f_s", _c_i32)]
+
+
+class RouteOutC(ctypes.Structure):
+    _fields_ = [("ids", _c_ptr), ("w", _c_ptr), ("counts", _c_ptr), ("offsets", _c_ptr),
+                ("perm", _c_ptr), ("inv", _c_ptr), ("tiles", _c_ptr), ("n_tiles", _c_ptr),
+                ("err", _c_ptr), ("T", _c_i32), ("E", _c_i32), ("k", _c_i32),
+                ("block_m", _c_i32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+_SIGS = {
+    "moe_route_max_tiles": (_c_i32, [_c_i32, _c_i32, _c_i32, _c_i32]),
+    "moe_route_workspace_size": (_c_size, [_c_i32, _c_i32, _c_i32]),
+    "moe_ffn_workspace_size": (_c_size, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32]),
+    "moe_layer_workspace_size": (_c_size, [_c_i32] * 6),
+    "moe_route": (_c_i32, [_c_ptr, ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
+    "moe_expert_ffn": (_c_i32, [_c_ptr, _c_i32, _c_i32, ctypes.POINTER(Q4WeightsC),
+                                ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "moe_layer": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4WeightsC),
+                           ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "moe_get_device_error": (_c_i32, [_c_ptr, ctypes.POINTER(_c_i32), _c_ptr]),
+    "moe_status_string": (ctypes.c_char_p, [_c_i32]),
+    "moe_residual_rms": (_c_i32, [_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr]),
+    "moe_debug_dequant": (_c_i32, [_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr, _c_ptr]),
+    "moe_debug_mma": (_c_i32, [_c_i32, _c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr]),
+    "moe_debug_set_stage_events": (_c_i32, [ctypes.POINTER(_c_ptr), _c_i32]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libmoeq4.so (built in-tree); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run `python -m routing_q4_grouped_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().moe_status_string(s).decode()
+
+
+def _check(fn, s):
+    if s != MOE_OK:
+        raise MoeError(fn, s)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+# ----------------------------------------------------------------- host-side sizes
+
+def moe_route_max_tiles(T, E, k, block_m) -> int:
+    return lib().moe_route_max_tiles(T, E, k, block_m)
+
+
+def moe_route_workspace_size(T, E, k) -> int:
+    return lib().moe_route_workspace_size(T, E, k)
+
+
+def moe_ffn_workspace_size(T, k, d, f, f_s) -> int:
+    return lib().moe_ffn_workspace_size(T, k, d, f, f_s)
+
+
+def moe_layer_workspace_size(T, E, k, d, f, f_s) -> int:
+    return lib().moe_layer_workspace_size(T, E, k, d, f, f_s)
+
+
+# ------------------------------------------------------------------ device buffers
+
+@dataclasses.dataclass
+class DeviceWeights:
+    """One layer's packed weights resident on the GPU (torch tensors as storage)."""
+    E: int
+    d: int
+    f: int
+    f_s: int
+    tensors: dict
+
+    @classmethod
+    def from_host(cls, W, device="cuda"):
+        """Copies a :class:`routing_q4_grouped_gb300.synth.Q4Weights` to the device."""
+        names = ["gu_qw", "gu_scale", "gu_bias", "dn_qw", "dn_scale", "dn_bias"]
+        if W.f_s:
+            names += ["sgu_qw", "sgu_scale", "sgu_bias", "sdn_qw", "sdn_scale", "sdn_bias"]
+        ts = {}
+        for n in names:
+            a = getattr(W, n)
+            t = torch.from_numpy(a.view(a.dtype.str.replace("u", "i")) if a.dtype.kind == "u" else a)
+            ts[n] = t.to(device)
+        return cls(W.E, W.d, W.f, W.f_s, ts)
+
+    def cstruct(self) -> Q4WeightsC:
+        t = self.tensors
+        m = lambda p: Q4Mat(_ptr(t.get(p + "_qw")), _ptr(t.get(p + "_scale")), _ptr(t.get(p + "_bias")))
+        return Q4WeightsC(m("gu"), m("dn"), m("sgu") if self.f_s else Q4Mat(),
+                          m("sdn") if self.f_s else Q4Mat(), self.E, self.d, self.f, self.f_s)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.tensors.values())
+
+
+@dataclasses.dataclass
+class RouteBuffers:
+    """Device arrays of a routing result (see moe_route_out in moeq4.h)."""
+    T: int
+    E: int
+    k: int
+    block_m: int
+    ids: torch.Tensor
+    w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    perm: torch.Tensor
+    inv: torch.Tensor
+    tiles: torch.Tensor
+    n_tiles: torch.Tensor
+    err: torch.Tensor
+
+    @classmethod
+    def alloc(cls, T, E, k, block_m=128, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        nmax = max(1, moe_route_max_tiles(T, E, k, block_m))
+        return cls(T, E, k, block_m,
+                   ids=torch.empty((T, k), **i32),
+                   w=torch.empty((T, k), dtype=torch.float32, device=device),
+                   counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                   perm=torch.empty(max(1, T * k), **i32), inv=torch.empty(max(1, T * k), **i32),
+                   tiles=torch.empty((nmax, 3), **i32), n_tiles=torch.zeros(4, **i32),
+                   err=torch.zeros(4, **i32))
+
+    def cstruct(self) -> RouteOutC:
+        return RouteOutC(_ptr(self.ids), _ptr(self.w), _ptr(self.counts), _ptr(self.offsets),
+                         _ptr(self.perm), _ptr(self.inv), _ptr(self.tiles), _ptr(self.n_tiles),
+                         _ptr(self.err), self.T, self.E, self.k, self.block_m)
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled scratch (the routing part must start zeroed)."""
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------- compute
+
+def moe_route(logits: torch.Tensor, out: RouteBuffers, ws: torch.Tensor, stream=None) -> None:
+    """Routing of fp32 logits [T, E] into ``out`` (asynchronous)."""
+    assert logits.dtype == torch.float32 and logits.is_contiguous()
+    c = out.cstruct()
+    _check("moe_route", lib().moe_route(_ptr(logits), ctypes.byref(c), _ptr(ws), ws.numel(),
+                                        _stream(stream)))
+
+
+def moe_expert_ffn(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.Tensor,
+                   ws: torch.Tensor, stream=None) -> None:
+    """Grouped expert FFN: bf16 x [T, d] -> bf16 y [T, d] (asynchronous)."""
+    assert x.dtype == torch.bfloat16 and y.dtype == torch.bfloat16
+    assert x.is_contiguous() and y.is_contiguous()
+    T, d = x.shape
+    wc, rc = W.cstruct(), r.cstruct()
+    _check("moe_expert_ffn", lib().moe_expert_ffn(_ptr(x), T, d, ctypes.byref(wc), ctypes.byref(rc),
+                                                  _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer(x: torch.Tensor, logits: torch.Tensor, W: DeviceWeights, r: RouteBuffers,
+              y: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """Routing then expert FFN on one stream, no host synchronisation."""
+    assert x.dtype == torch.bfloat16 and logits.dtype == torch.float32
+    T = x.shape[0]
+    wc, rc = W.cstruct(), r.cstruct()
+    _check("moe_layer", lib().moe_layer(_ptr(x), _ptr(logits), T, ctypes.byref(wc), ctypes.byref(rc),
+                                        _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_residual_rms(y: torch.Tensor, x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Next layer's input of the chunked run: bf16((y + x) / rms(y + x)) per token."""
+    T, d = x.shape
+    _check("moe_residual_rms", lib().moe_residual_rms(_ptr(y), _ptr(x), _ptr(out), T, d,
+                                                      _stream(stream)))
+
+
+def moe_get_device_error(r: RouteBuffers, stream=None) -> int:
+    """Synchronises the stream and returns the device error word (0 = none)."""
+    code = _c_i32(0)
+    s = lib().moe_get_device_error(_ptr(r.err), ctypes.byref(code), _stream(stream))
+    if s not in (MOE_OK, -5):
+        raise MoeError("moe_get_device_error", s)
+    return code.value
+
+
+# ----------------------------------------------------------------- test-only calls
+
+def moe_debug_dequant(qw, scale, bias, out, stream=None) -> None:
+    rows, K = out.shape
+    _check("moe_debug_dequant", lib().moe_debug_dequant(_ptr(qw), _ptr(scale), _ptr(bias), rows, K,
+                                                        _ptr(out), _stream(stream)))
+
+
+def moe_debug_mma(a_from_tmem: bool, A, B, D, stream=None) -> None:
+    N, K = B.shape
+    _check("moe_debug_mma", lib().moe_debug_mma(int(a_from_tmem), _ptr(A), _ptr(B), _ptr(D), N, K,
+                                                _stream(stream)))
+
+
+def moe_debug_set_stage_events(events) -> None:
+    """Registers torch.cuda.Event objects recorded at the layer's stage boundaries."""
+    arr = (_c_ptr * max(1, len(events)))(*[e.cuda_event for e in events])
+    _check("moe_debug_set_stage_events", lib().moe_debug_set_stage_events(arr, len(events)))
+
+
+class Layer:
+    """Convenience owner of the buffers one layer call needs (T tokens)."""
+
+    def __init__(self, W: DeviceWeights, T: int, k: int, block_m: int = 128, device="cuda"):
+        self.W, self.T, self.k = W, T, k
+        self.route = RouteBuffers.alloc(T, W.E, k, block_m, device)
+        self.ws = alloc_workspace(moe_layer_workspace_size(T, W.E, k, W.d, W.f, W.f_s), device)
+        self.y = torch.empty((T, W.d), dtype=torch.bfloat16, device=device)
+
+    def __call__(self, x, logits, stream=None):
+        moe_layer(x, logits, self.W, self.route, self.y, self.ws, stream)
+        return self.y

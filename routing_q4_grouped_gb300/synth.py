@@ -120,10 +120,10 @@ CONFIGS = {
 }
 
 
-def gen_x(cfg: Config, T: int | None = None) -> np.ndarray:
-    """Token activations, bf16 bits [T, d]."""
+def gen_x(cfg: Config, T: int | None = None, layer: int = 0) -> np.ndarray:
+    """Token activations, bf16 bits [T, d] (``layer`` selects an independent draw)."""
     T = cfg.T if T is None else T
-    return to_bf16_bits(normal(cfg.seed, TID["x"], 0, T * cfg.d).reshape(T, cfg.d))
+    return to_bf16_bits(normal(cfg.seed, TID["x"], layer, T * cfg.d).reshape(T, cfg.d))
 
 
 def gen_logits(cfg: Config, layer: int = 0, T: int | None = None) -> np.ndarray:

@@ -1,0 +1,81 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol the
+headers declare, and rejects bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("moeq4.h", "moeq4_debug.h")]
+
+
+@pytest.fixture(scope="module")
+def L():
+    from routing_q4_grouped_gb300 import build, moeq4
+    if not os.path.exists(moeq4.LIB_PATH):
+        build.build()
+    return moeq4
+
+
+def _declared():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*[a-zA-Z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_headers_declare_the_boundary():
+    names = _declared()
+    for n in ("moe_route", "moe_expert_ffn", "moe_layer", "moe_route_max_tiles",
+              "moe_route_workspace_size", "moe_ffn_workspace_size", "moe_layer_workspace_size",
+              "moe_get_device_error", "moe_status_string", "moe_residual_rms", "moe_debug_dequant", "moe_debug_mma",
+              "moe_debug_set_stage_events"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = ctypes.CDLL(L.LIB_PATH)
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_side_sizes(L):
+    assert L.moe_route_max_tiles(4096, 256, 8, 128) == 4096 * 8 // 128 + 256
+    assert L.moe_route_max_tiles(3, 4, 2, 2) == 3 + 4
+    assert L.moe_route_workspace_size(4096, 256, 8) > 4096 * 8 * 4
+    ffn = L.moe_ffn_workspace_size(4096, 8, 2048, 512, 512)
+    assert ffn >= 4096 * 8 * 512 * 2 + 4096 * 512 * 2 + 4096 * 2048 * 4
+    lay = L.moe_layer_workspace_size(4096, 256, 8, 2048, 512, 512)
+    assert lay >= ffn + L.moe_route_workspace_size(4096, 256, 8)
+    assert L.status_string(0) == "ok"
+    assert "workspace" in L.status_string(-3)
+
+
+def test_bad_arguments_rejected_on_host(L):
+    lib = L.lib()
+    r = L.RouteOutC()                       # all NULL
+    r.T, r.E, r.k, r.block_m = 16, 8, 2, 128
+    assert lib.moe_route(None, ctypes.byref(r), None, 0, None) == -1      # MOE_ERR_ARG
+    fake = 1 << 20                          # aligned non-null values, never dereferenced
+    for f in ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "n_tiles", "err"):
+        setattr(r, f, fake)
+    r.k = 9                                 # k > E
+    assert lib.moe_route(fake, ctypes.byref(r), fake, 1 << 30, None) == -1
+    r.k, r.block_m = 2, 129                 # block_m above the supported maximum
+    assert lib.moe_route(fake, ctypes.byref(r), fake, 1 << 30, None) == -1
+    r.block_m = 128
+    assert lib.moe_route(fake, ctypes.byref(r), fake, 0, None) == -3      # workspace too small
+    assert lib.moe_route(fake + 4, ctypes.byref(r), fake, 1 << 30, None) == -7   # misaligned
+    W = L.Q4WeightsC()
+    W.E, W.d, W.f, W.f_s = 8, 200, 128, 0   # d not a multiple of 128
+    for m in (W.gate_up, W.down):
+        m.qw = m.scale = m.bias = fake
+    assert lib.moe_expert_ffn(fake, 16, 200, ctypes.byref(W), ctypes.byref(r), fake, fake,
+                              1 << 30, None) == -2
+    W.d, W.f_s = 256, 128                    # shared expert declared but pointers NULL
+    assert lib.moe_expert_ffn(fake, 16, 256, ctypes.byref(W), ctypes.byref(r), fake, fake,
+                              1 << 30, None) == -1
