@@ -299,6 +299,9 @@ def run_ours(args):
     # ---- per-kernel times over the same K steps, stage events on the launching stream
     stage_ms = {s: [] for s in STAGES}
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for row in evs:             # torch creates the CUDA event on first record
+        for e in row:
+            e.record(stream)
     torch.cuda.synchronize()
     for i in range(args.steps):
         moeq4.moe_debug_set_stage_events(evs[i])
