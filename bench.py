@@ -263,7 +263,7 @@ def run_ours(args):
         lg = torch.from_numpy(l_h).cuda()
         sets.append((W, x, lg, x_h, l_h))
     route = moeq4.RouteBuffers.alloc(T, E, k, args.block_m)
-    ws = moeq4.alloc_workspace(moeq4.moe_layer_workspace_size(T, E, k, d, f, fs))
+    ws = moeq4.alloc_workspace(moeq4.moe_layer_workspace_size(T, E, k, d, f, fs, args.block_m))
     y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
     weight_bytes = sets[0][0].nbytes
 

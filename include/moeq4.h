@@ -112,13 +112,16 @@ int32_t moe_route_max_tiles(int32_t T, int32_t E, int32_t k, int32_t block_m);
  * first use; every moe_route call leaves it zero-filled again. */
 size_t moe_route_workspace_size(int32_t T, int32_t E, int32_t k);
 
-/* Bytes of scratch for moe_expert_ffn (no zero-fill requirement). */
-size_t moe_ffn_workspace_size(int32_t T, int32_t k, int32_t d, int32_t f, int32_t f_s);
+/* Bytes of scratch for moe_expert_ffn (no zero-fill requirement): the SwiGLU
+ * activations of every routed row (tile-padded to 16 rows), those of the shared
+ * expert, and the fp32 combine buffer [T][d]. */
+size_t moe_ffn_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
+                              int32_t f_s, int32_t block_m);
 
 /* Bytes of scratch for moe_layer: the routing part followed by the FFN part.
  * Zero-fill it before first use (the routing part must start zeroed). */
 size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
-                                int32_t f_s);
+                                int32_t f_s, int32_t block_m);
 
 /* Routing on the GPU, enqueued on one stream with no host synchronisation
  * ([A] §5-2: histogram, prefix scan, scatter and block map in one command
@@ -141,7 +144,7 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  *   W   layer weights (host struct, device arrays), W->d must equal d
  *   r   routing result of moe_route for the same T (device arrays)
  *   y   bf16 [T][d] output (device)
- *   ws  scratch of moe_ffn_workspace_size(T, k, d, f, f_s) bytes */
+ *   ws  scratch of moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m) bytes */
 moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weights* W,
                           const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream);

@@ -32,6 +32,13 @@ moe_status moe_debug_dequant(const uint32_t* qw, const uint16_t* scale, const ui
 moe_status moe_debug_mma(int32_t a_from_tmem, const uint16_t* A, const uint16_t* B, float* D,
                          int32_t N, int32_t K, void* stream);
 
+/* Tensor-memory fragment check: every lane L of a 128-lane allocation holds
+ * (L << 16 | c) in columns c = 0..31 (written with the 32x32b shape); warp q
+ * reads lanes 32q..32q+15 and 32q+16..32q+31 back with the 16x256b shape.
+ *   out uint32 [128][32]: out[(32q + t)*32 + i] = register i of thread t of warp q,
+ *   registers 0..15 from the first read, 16..31 from the second. */
+moe_status moe_debug_tmem_layout(uint32_t* out, void* stream);
+
 /* Stage timing for benchmarks: with n > 0, moe_route / moe_expert_ffn /
  * moe_layer record events[i] (cudaEvent_t handles created by the caller) on
  * the call's stream at stage boundaries: 0 before routing, 1 after selection +

@@ -179,13 +179,19 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weight
   if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_ALIGN;
   if (T != r->T || d != W->d || W->E != r->E) return MOE_ERR_SHAPE;
   const int k = r->k, E = W->E, f = W->f, fs = W->f_s;
-  const FfnWs L = ffn_ws_layout(T, k, d, f, fs);
+  const int max_tiles = moe_route_max_tiles(T, E, k, r->block_m);
+  const FfnWs L = ffn_ws_layout(T, k, d, f, fs, max_tiles);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   DevInfo di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   if (T == 0) return MOE_OK;
 
   char* base = static_cast<char*>(ws);
+  uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
+  uint16_t* act_sh = reinterpret_cast<uint16_t*>(base + L.act_sh);
+  const uint64_t act_rows = act_rows_capacity(T, k, max_tiles);
+  const uint64_t act_sh_rows = (static_cast<uint64_t>(T) + gemm_tile_rows() - 1) /
+                               gemm_tile_rows() * gemm_tile_rows();
   GemmArgs a{};
   a.E = E;
   a.T = T;
@@ -195,16 +201,14 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weight
   a.f_s = fs;
   a.tiles = r->tiles;
   a.n_tiles = r->n_tiles;
-  a.max_tiles = moe_route_max_tiles(T, E, k, r->block_m);
+  a.max_tiles = max_tiles;
   a.perm = r->perm;
   a.wts = r->w;
-  a.act = reinterpret_cast<uint16_t*>(base + L.act);
-  a.act_sh = reinterpret_cast<uint16_t*>(base + L.act_sh);
   a.y_acc = reinterpret_cast<float*>(base + L.y_acc);
   a.err = r->err;
   a.timeout_ns = timeout_ns();
+  const int n_sh_tiles = fs ? (T + gemm_tile_rows() - 1) / gemm_tile_rows() : 0;
 
-  CUtensorMap tmA, tmA_sh, tmB, tmB_sh;
   const CUtensorMapSwizzle SW32 = CU_TENSOR_MAP_SWIZZLE_32B, SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
   const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -212,49 +216,59 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weight
   // ---- pass 0: gate/up + SwiGLU
   {
     GemmArgs g = a;
+    GemmMaps m;
     g.K = d;
     g.K_sh = d;
-    g.n_fb = f / 128;
-    g.n_fb_sh = fs / 128;
-    g.n_sh_tiles = fs ? (T + gemm_tile_rows(0) - 1) / gemm_tile_rows(0) : 0;
+    g.n_fb = f / 64;
+    g.n_fb_sh = fs / 64;
+    g.n_sh_tiles = n_sh_tiles;
     g.scale = W->gate_up.scale;
     g.bias = W->gate_up.bias;
     g.sh_scale = fs ? W->sh_gate_up.scale : W->gate_up.scale;
     g.sh_bias = fs ? W->sh_gate_up.bias : W->gate_up.bias;
-    bool ok = encode_2d(&tmA, U32, 4, W->gate_up.qw, d / 8, static_cast<uint64_t>(E) * 2 * f, 8,
-                        128, SW32) &&
-              encode_2d(&tmB, BF16, 2, x, d, T, 64, 1, SW128);
-    if (fs) ok = ok && encode_2d(&tmA_sh, U32, 4, W->sh_gate_up.qw, d / 8, 2ull * fs, 8, 128, SW32);
-    else tmA_sh = tmA;
-    tmB_sh = tmB;
+    bool ok = encode_2d(&m.A, U32, 4, W->gate_up.qw, d / 8, static_cast<uint64_t>(E) * 2 * f, 8,
+                        64, SW32) &&
+              encode_2d(&m.B, BF16, 2, x, d, T, 64, 1, SW128) &&
+              encode_2d(&m.C, BF16, 2, act, f, act_rows, 64, 16, SW128);
+    if (fs)
+      ok = ok && encode_2d(&m.A_sh, U32, 4, W->sh_gate_up.qw, d / 8, 2ull * fs, 8, 64, SW32) &&
+           encode_2d(&m.C_sh, BF16, 2, act_sh, fs, act_sh_rows, 64, 16, SW128);
+    else {
+      m.A_sh = m.A;
+      m.C_sh = m.C;
+    }
+    m.B_sh = m.B;
     if (!ok) return MOE_ERR_CUDA;
-    if (launch_gemm(0, g, tmA, tmA_sh, tmB, tmB_sh, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(0, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
     stage_mark(3, s);
   }
   // ---- pass 1: down + weighted combine (+ shared expert)
   {
     GemmArgs g = a;
+    GemmMaps m;
     g.K = f;
     g.K_sh = fs;
     g.n_fb = d / 128;
     g.n_fb_sh = fs ? d / 128 : 0;
-    g.n_sh_tiles = fs ? (T + gemm_tile_rows(1) - 1) / gemm_tile_rows(1) : 0;
+    g.n_sh_tiles = n_sh_tiles;
     g.scale = W->down.scale;
     g.bias = W->down.bias;
     g.sh_scale = fs ? W->sh_down.scale : W->down.scale;
     g.sh_bias = fs ? W->sh_down.bias : W->down.bias;
-    bool ok = encode_2d(&tmA, U32, 4, W->down.qw, f / 8, static_cast<uint64_t>(E) * d, 8, 128,
+    bool ok = encode_2d(&m.A, U32, 4, W->down.qw, f / 8, static_cast<uint64_t>(E) * d, 8, 64,
                         SW32) &&
-              encode_2d(&tmB, BF16, 2, a.act, f, static_cast<uint64_t>(T) * k, 64, 16, SW128);
+              encode_2d(&m.B, BF16, 2, act, f, act_rows, 64, 16, SW128);
     if (fs)
-      ok = ok && encode_2d(&tmA_sh, U32, 4, W->sh_down.qw, fs / 8, d, 8, 128, SW32) &&
-           encode_2d(&tmB_sh, BF16, 2, a.act_sh, fs, T, 64, 16, SW128);
+      ok = ok && encode_2d(&m.A_sh, U32, 4, W->sh_down.qw, fs / 8, d, 8, 64, SW32) &&
+           encode_2d(&m.B_sh, BF16, 2, act_sh, fs, act_sh_rows, 64, 16, SW128);
     else {
-      tmA_sh = tmA;
-      tmB_sh = tmB;
+      m.A_sh = m.A;
+      m.B_sh = m.B;
     }
+    m.C = m.B;
+    m.C_sh = m.B_sh;
     if (!ok) return MOE_ERR_CUDA;
-    if (launch_gemm(1, g, tmA, tmA_sh, tmB, tmB_sh, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(1, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
     stage_mark(4, s);
   }
   if (launch_finalize(a.y_acc, y, static_cast<size_t>(T) * d, s) != cudaSuccess)
@@ -295,14 +309,16 @@ size_t moe_route_workspace_size(int32_t T, int32_t E, int32_t k) {
   return route_ws_layout(T, E, k).total;
 }
 
-size_t moe_ffn_workspace_size(int32_t T, int32_t k, int32_t d, int32_t f, int32_t f_s) {
-  if (T < 0 || k < 1 || d < 1 || f < 1 || f_s < 0) return 0;
-  return ffn_ws_layout(T, k, d, f, f_s).total;
+size_t moe_ffn_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
+                              int32_t f_s, int32_t block_m) {
+  if (T < 0 || E < 1 || k < 1 || d < 1 || f < 1 || f_s < 0 || block_m < 1) return 0;
+  return ffn_ws_layout(T, k, d, f, f_s, moe_route_max_tiles(T, E, k, block_m)).total;
 }
 
 size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
-                                int32_t f_s) {
-  const size_t a = moe_route_workspace_size(T, E, k), b = moe_ffn_workspace_size(T, k, d, f, f_s);
+                                int32_t f_s, int32_t block_m) {
+  const size_t a = moe_route_workspace_size(T, E, k);
+  const size_t b = moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m);
   if (!a || !b) return 0;
   return align256(a) + b;
 }
@@ -323,7 +339,7 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
                      void* stream) {
   if (!W || !r) return MOE_ERR_ARG;
   if (r->T != T) return MOE_ERR_SHAPE;
-  const size_t need = moe_layer_workspace_size(T, r->E, r->k, W->d, W->f, W->f_s);
+  const size_t need = moe_layer_workspace_size(T, r->E, r->k, W->d, W->f, W->f_s, r->block_m);
   if (!ws || need == 0 || ws_bytes < need) return MOE_ERR_WORKSPACE;
   const size_t rsz = align256(moe_route_workspace_size(T, r->E, r->k));
   moe_status st;

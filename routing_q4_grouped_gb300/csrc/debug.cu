@@ -112,10 +112,48 @@ __global__ void __launch_bounds__(128, 1) mma_probe_kernel(int a_tmem, const uin
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Each lane L writes (L << 16 | column) into columns 0..31 with the 32x32b shape;
+// warp q then reads lanes 32q.. and 32q+16.. back with the 16x256b shape.
+// out[(q*32 + t)*32 + i] = register i of thread t (first load: i < 16).
+__global__ void __launch_bounds__(128, 1) tmem_layout_probe_kernel(uint32_t* out) {
+  __shared__ uint32_t tbase;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    tmem_alloc(&tbase, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  uint32_t v[16];
+  for (int half = 0; half < 2; ++half) {
+    for (int i = 0; i < 16; ++i) v[i] = (static_cast<uint32_t>(tid) << 16) | (half * 16 + i);
+    tmem_st_32x32b_x16(tbase + lane_base + half * 16, v);
+  }
+  tmem_st_wait();
+  uint32_t r[16];
+  for (int half = 0; half < 2; ++half) {
+    tmem_ld_16x256b_x4(tbase + lane_base + (static_cast<uint32_t>(half * 16) << 16), r);
+    tmem_ld_wait();
+    for (int i = 0; i < 16; ++i) out[static_cast<size_t>(tid) * 32 + half * 16 + i] = r[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 32);
+}
+
 }  // namespace
 }  // namespace moeq4
 
 using namespace moeq4;
+
+extern "C" moe_status moe_debug_tmem_layout(uint32_t* out, void* stream) {
+  if (!out) return MOE_ERR_ARG;
+  tmem_layout_probe_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(out);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 extern "C" moe_status moe_debug_dequant(const uint32_t* qw, const uint16_t* scale,
                                         const uint16_t* bias, int32_t rows, int32_t K,

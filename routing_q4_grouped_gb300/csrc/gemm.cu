@@ -4,25 +4,34 @@
 // tile by tile in on-chip memory and accumulates in FP32; "Apple silicon용
 // Lily, Qwen 추론 최적화" (aitrends.kr), section "Qwen 구조와 Prefill 경로").
 //
-// Orientation (weights as the MMA's M side): D[features, tokens] = W[features, K]
-// * X[tokens, K]^T with M = 128 output features, N = the tile's rows (padded to
-// 16) and K chunks of 64 = one quantisation group. The dequantised weights go
-// from registers straight into tensor memory (tcgen05.st) and feed the MMA as
-// its A operand, so no bf16 weight tile ever touches shared or global memory.
-// Token rows arrive by TMA (gather4 of x rows for the gate/up pass, plain 2D
-// tiles of the permuted activation rows for the down pass).
+// Orientation (weights on the MMA's M side): D[features, tokens] = W[features, K]
+// * X[tokens, K]^T, M = 128 weight rows, N = the tile's rows padded to 16 (<= 128),
+// K in chunks of 64 = one quantisation group. Dequantised weights go from
+// registers into tensor memory (tcgen05.st) and feed the MMA as operand A, so no
+// bf16 weight tile touches shared or global memory. Token rows arrive by TMA:
+// gather4 of x rows for the gate/up pass, 16-row tiles of the (tile-padded)
+// activation rows for the down pass.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over units):
-//   warps 0-7  dequantise packed codes -> TMEM A stages; then the epilogue
-//   warp 8     TMA producer (packed codes + token rows into a smem ring)
-//   warp 9     TMEM allocator and single-thread MMA issuer
-// Unit = (block-map tile or shared-expert tile, feature block).
+// Warp roles (448 threads, one CTA per SM, persistent over units):
+//   warps 0-7   dequantisation; warp w serves TMEM lane quarter w%4 and the
+//               K-chunks of parity w/4 of every unit
+//   warps 8-11  epilogue (lane quarter w-8), overlapped with the next unit's
+//               mainloop through two accumulator buffers
+//   warp 12     TMA producer (packed codes + token rows into a 6-stage ring)
+//   warp 13     TMEM allocator and single-thread MMA issuer
+// Tensor memory: columns [0, 256) hold 8 A stages of 32 columns (128 rows x 64
+// bf16), [256, 512) two 128-column fp32 accumulators.
 //
-// Pass 0 (gate/up): A = 128 gate rows and the matching 128 up rows, two MMAs
-//   per K step into two accumulators on the same TMEM lanes, so each epilogue
-//   thread holds gate_i and up_i: act = bf16(silu(gate) * up). Also zeroes y_acc.
-// Pass 1 (down): A = 128 rows of the down matrix, B = act rows of the tile;
-//   epilogue y_acc[t] += w[t, j] * D (fp32 reductions); shared expert weight 1.
+// Pass 0 (gate/up): a unit covers 64 output features; its A tile interleaves
+//   the gate and up rows in blocks of 8 (TMEM lanes 16m..16m+7 = gate features
+//   8m.., lanes 16m+8.. = the matching up features), so one 16x256b tensor-memory
+//   load gives each epilogue thread gate and up values of the same feature and
+//   token: act = bf16(silu(gate) * up), staged in shared memory and written with
+//   TMA tile stores. This pass also zeroes the fp32 combine buffer.
+// Pass 1 (down): a unit covers 128 output features of the tile's rows; the
+//   epilogue scales each token column by its routing weight (1 for the shared
+//   expert) and adds the 512-byte row slices into y_acc with asynchronous bulk
+//   reduce-add copies.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -36,71 +45,54 @@ namespace moeq4 {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kDqWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kNMax = 128;                 // rows per unit (MMA N)
+constexpr int kStages = 6;                 // shared-memory ring depth
+constexpr int kAStages = 8;                // TMEM A stages
+constexpr int kACols = 32;                 // TMEM columns per A stage
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = 256;   // accumulators live in columns [256, 512)
+constexpr uint32_t kDCol = 256;            // accumulator buffer b at column 256 + 128 b
+constexpr int kDqWarps = 8;
+constexpr int kEpiWarp0 = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
+static_assert(kThreads == kGemmThreads, "thread count");
 
-template <int MODE>
-struct Cfg;
-template <>
-struct Cfg<0> {                       // gate/up + SwiGLU
-  static constexpr int kNMax = 128;   // tile rows (two accumulators of N columns)
-  static constexpr int kStages = 6;   // smem ring depth
-  static constexpr int kAStages = 4;  // TMEM A stages
-  static constexpr int kACols = 64;   // TMEM columns per A stage (gate 32 + up 32)
-  static constexpr int kARows = 256;  // packed rows per chunk (gate 128 + up 128)
-};
-template <>
-struct Cfg<1> {                       // down + weighted combine
-  static constexpr int kNMax = 256;
-  static constexpr int kStages = 5;
-  static constexpr int kAStages = 8;
-  static constexpr int kACols = 32;
-  static constexpr int kARows = 128;
-};
+constexpr int kBBytes = kNMax * 128;       // token rows: 64 bf16 (128 B) each, 128B swizzle
+constexpr int kABytes = 128 * 32;          // packed codes: 64 codes (32 B) per row, 32B swizzle
+constexpr int kEpiBytes = 32768;           // pass 0: act tile [128][64] bf16; pass 1: 2 x [32][128] fp32
+constexpr size_t kOffB = 0;
+constexpr size_t kOffA = kOffB + size_t(kStages) * kBBytes;
+constexpr size_t kOffEpi = kOffA + size_t(kStages) * kABytes;
+constexpr size_t kOffCtl = kOffEpi + kEpiBytes;
 
-template <int MODE>
-struct Layout {
-  using C = Cfg<MODE>;
-  static constexpr int kBBytes = C::kNMax * 128;   // token rows: 64 bf16 (128 B) each
-  static constexpr int kABytes = C::kARows * 32;   // packed codes: 64 codes (32 B) per row
-  static constexpr size_t kOffB = 0;
-  static constexpr size_t kOffA = kOffB + size_t(C::kStages) * kBBytes;
-  static constexpr size_t kOffCtl = kOffA + size_t(C::kStages) * kABytes;
-};
-
-template <int MODE>
 struct Ctl {
-  uint64_t full[Cfg<MODE>::kStages];
-  uint64_t empty[Cfg<MODE>::kStages];
-  uint64_t a_full[Cfg<MODE>::kAStages];
-  uint64_t a_empty[Cfg<MODE>::kAStages];
-  uint64_t d_full, d_empty, drain;
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t a_full[kAStages];
+  uint64_t a_empty[kAStages];
+  uint64_t d_full[2];
+  uint64_t d_empty[2];
+  uint64_t epi_bar;
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int zero;
-  int tok[Cfg<MODE>::kNMax];
+  int tok[kNMax];      // producer: x rows to gather (pass 0)
+  int e_tok[2][kNMax];    // epilogue: token of each row (pass 1), -1 = padding; per unit parity
+  float e_w[2][kNMax];    // epilogue: routing weight of each row (pass 1)
 };
 
-template <int MODE>
-constexpr size_t smem_bytes() {
-  return 1024 + Layout<MODE>::kOffCtl + sizeof(Ctl<MODE>);
-}
+constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Ctl);
 
 struct Unit {
   int e, row0, rows, fb, K;
+  int act0;    // first activation row of the tile (16-aligned, tile-padded layout)
   bool shared;
 };
 
-template <int MODE>
-__device__ __forceinline__ int shared_tile_rows() {
-  return Cfg<MODE>::kNMax;
-}
-
-// Unit u -> (tile, feature block). Routed units first (tile-major), then shared.
-template <int MODE>
+// Unit u -> (tile, feature block). Routed units first, tile-major, then shared.
 __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, Unit& U) {
   const int n_routed = n_rt * a.n_fb;
   if (u < n_routed) {
@@ -112,7 +104,8 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
     U.rows = __ldg(tl + 2);
     U.shared = false;
     U.K = a.K;
-    if (U.e < 0 || U.e >= a.E || U.rows < 1 || U.rows > Cfg<MODE>::kNMax || U.row0 < 0 ||
+    U.act0 = act_tile_base(U.row0, ti);
+    if (U.e < 0 || U.e >= a.E || U.rows < 1 || U.rows > kNMax || U.row0 < 0 ||
         static_cast<long long>(U.row0) + U.rows > static_cast<long long>(a.T) * a.k)
       return false;
   } else {
@@ -120,61 +113,85 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
     const int st = v / a.n_fb_sh;
     U.fb = v - st * a.n_fb_sh;
     U.e = 0;
-    U.row0 = st * shared_tile_rows<MODE>();
-    U.rows = min(shared_tile_rows<MODE>(), a.T - U.row0);
+    U.row0 = st * kNMax;
+    U.rows = min(kNMax, a.T - U.row0);
     U.shared = true;
     U.K = a.K_sh;
+    U.act0 = U.row0;
   }
   return true;
 }
 
-// First packed-matrix row of A's two 128-row halves (gate / up) or of its only half.
+// First packed-matrix rows of the unit's two 64-row halves of A.
 template <int MODE>
 __device__ __forceinline__ void a_rows(const GemmArgs& a, const Unit& U, int& r0, int& r1) {
   if (MODE == 0) {
     const int F = U.shared ? a.f_s : a.f;
-    r0 = U.e * 2 * F + U.fb * 128;
-    r1 = r0 + F;
+    r0 = U.e * 2 * F + U.fb * 64;   // gate rows
+    r1 = r0 + F;                    // the matching up rows
   } else {
     r0 = U.e * a.d + U.fb * 128;
-    r1 = r0;
+    r1 = r0 + 64;
   }
 }
 
+// TMEM lane L of the unit's A tile -> row of the packed shared-memory tile.
 template <int MODE>
-__device__ __forceinline__ void raise_abort(Ctl<MODE>& ctl, int32_t* err) {
+__device__ __forceinline__ int lane_to_srow(int L) {
+  if (MODE == 0) return ((L >> 3) & 1) * 64 + 8 * (L >> 4) + (L & 7);
+  return L;
+}
+
+__device__ __forceinline__ void raise_abort(Ctl& ctl, int32_t* err) {
   if (atomicExch(&ctl.abort, 1) == 0) atomicOr(err, MOE_DEVERR_PIPE_TIMEOUT);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// Bounded barrier of the four epilogue warps (an mbarrier with 4 arrivals).
+__device__ __forceinline__ bool epi_sync(Ctl& ctl, uint32_t& phase, uint64_t limit) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.epi_bar);
+  const bool ok = __all_sync(kFull, mbar_wait(&ctl.epi_bar, phase, &ctl.abort, limit));
+  phase ^= 1u;
+  return ok;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
 
 template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     q4_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmA_sh,
                            const __grid_constant__ CUtensorMap tmB,
-                           const __grid_constant__ CUtensorMap tmB_sh, const GemmArgs a) {
-  using C = Cfg<MODE>;
-  using L = Layout<MODE>;
+                           const __grid_constant__ CUtensorMap tmB_sh,
+                           const __grid_constant__ CUtensorMap tmC,
+                           const __grid_constant__ CUtensorMap tmC_sh, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sB = smem + L::kOffB;
-  uint8_t* sA = smem + L::kOffA;
-  Ctl<MODE>& ctl = *reinterpret_cast<Ctl<MODE>*>(smem + L::kOffCtl);
+  uint8_t* sB = smem + kOffB;
+  uint8_t* sA = smem + kOffA;
+  uint8_t* sEpi = smem + kOffEpi;
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], kDqWarps + 1);
+      mbar_init(&ctl.empty[s], kDqWarps / 2 + 1);
     }
-    for (int s = 0; s < C::kAStages; ++s) {
-      mbar_init(&ctl.a_full[s], kDqWarps);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&ctl.a_full[s], kDqWarps / 2);
       mbar_init(&ctl.a_empty[s], 1);
     }
-    mbar_init(&ctl.d_full, 1);
-    mbar_init(&ctl.d_empty, kDqWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl.d_full[b], 1);
+      mbar_init(&ctl.d_empty[b], kEpiWarps);
+    }
+    mbar_init(&ctl.epi_bar, kEpiWarps);
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
     ctl.zero = 0;
@@ -195,6 +212,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const volatile int* abortp = &ctl.abort;
+  const uint64_t lim = a.timeout_ns;
 
   int n_rt = __ldg(a.n_tiles);
   if (n_rt < 0 || n_rt > a.max_tiles) {
@@ -205,13 +223,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    const uint64_t pol_w = policy_evict_first();   // weights: streamed once
-    const uint64_t pol_x = policy_evict_last();    // token rows: reused across units
+    const uint64_t pol_x = policy_evict_last();   // token rows: reused by every feature block
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
-      if (!decode_unit<MODE>(a, n_rt, u, U)) {
+      if (!decode_unit(a, n_rt, u, U)) {
         if (lane == 0) atomicOr(a.err, MOE_DEVERR_BAD_TILE);
         continue;
       }
@@ -227,22 +244,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
       }
-      const uint32_t bytes = L::kABytes + npad * 128;
+      const uint32_t bytes = kABytes + npad * 128;
       const int nch = U.K / 64;
       for (int c = 0; c < nch; ++c, ++it) {
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1u;
-        if (!__all_sync(kFull, mbar_wait(&ctl.empty[s], ph ^ 1u, abortp, a.timeout_ns))) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        if (!__all_sync(kFull, mbar_wait(&ctl.empty[s], ph ^ 1u, abortp, lim))) {
           if (lane == 0) raise_abort(ctl, a.err);
           ok = false;
           break;
         }
-        uint8_t* dA = sA + s * L::kABytes;
-        uint8_t* dB = sB + s * L::kBBytes;
+        uint8_t* dA = sA + s * kABytes;
+        uint8_t* dB = sB + s * kBBytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(&ctl.full[s], bytes);
-          tma_load_2d(dA, mA, &ctl.full[s], c * 8, r0, pol_w);
-          if (MODE == 0) tma_load_2d(dA + 128 * 32, mA, &ctl.full[s], c * 8, r1, pol_w);
+          tma_load_2d(dA, mA, &ctl.full[s], c * 8, r0, 0);
+          tma_load_2d(dA + 64 * 32, mA, &ctl.full[s], c * 8, r1, 0);
         }
         __syncwarp();
         if (MODE == 0) {
@@ -251,16 +268,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         ctl.tok[4 * g + 1], ctl.tok[4 * g + 2], ctl.tok[4 * g + 3], pol_x);
         } else {
           for (int g = lane; g < npad / 16; g += 32)
-            tma_load_2d(dB + g * 2048, mB, &ctl.full[s], c * 64, U.row0 + 16 * g, pol_x);
+            tma_load_2d(dB + g * 2048, mB, &ctl.full[s], c * 64, U.act0 + 16 * g, pol_x);
         }
       }
     }
     if (!ok && lane == 0) {
       // let copies already in flight land before the CTA's shared memory goes away
-      const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
+      const uint32_t n = it < static_cast<uint32_t>(kStages) ? it : kStages;
       for (uint32_t i = 1; i <= n; ++i) {
         const uint32_t j = it - i;
-        mbar_wait(&ctl.full[j % C::kStages], (j / C::kStages) & 1u, &ctl.zero, 20000000ull);
+        mbar_wait(&ctl.full[j % kStages], (j / kStages) & 1u, &ctl.zero, 20000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -270,103 +287,92 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         Unit U;
-        if (!decode_unit<MODE>(a, n_rt, u, U)) continue;
+        if (!decode_unit(a, n_rt, u, U)) continue;
         const uint32_t npad = (U.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(128, npad);
-        if (!mbar_wait(&ctl.d_empty, (nu & 1u) ^ 1u, abortp, a.timeout_ns)) {
+        const uint32_t db = nu & 1u;
+        if (!mbar_wait(&ctl.d_empty[db], ((nu >> 1) & 1u) ^ 1u, abortp, lim)) {
           raise_abort(ctl, a.err);
           break;
         }
         tc_fence_after();
+        const uint32_t dcol = tmem + kDCol + db * 128;
         const int nch = U.K / 64;
         for (int c = 0; c < nch; ++c, ++it, ++ita) {
-          const int s = it % C::kStages;
-          const uint32_t ph = (it / C::kStages) & 1u;
-          const int sa = ita % C::kAStages;
-          const uint32_t pha = (ita / C::kAStages) & 1u;
-          if (!mbar_wait(&ctl.full[s], ph, abortp, a.timeout_ns) ||
-              !mbar_wait(&ctl.a_full[sa], pha, abortp, a.timeout_ns)) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          const int sa = ita % kAStages;
+          const uint32_t pha = (ita / kAStages) & 1u;
+          if (!mbar_wait(&ctl.full[s], ph, abortp, lim) ||
+              !mbar_wait(&ctl.a_full[sa], pha, abortp, lim)) {
             raise_abort(ctl, a.err);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bsm = smem_u32(sB + s * L::kBBytes);
-          const uint32_t acol = tmem + sa * C::kACols;
+          const uint32_t bsm = smem_u32(sB + s * kBBytes);
+          const uint32_t acol = tmem + sa * kACols;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = sdesc_k_sw128(bsm + kk * 32);
-            const uint32_t acc = (c | kk) != 0;
-            mma_ts(tmem + kDCol, acol + kk * 8, bdesc, idesc, acc);
-            if (MODE == 0) mma_ts(tmem + kDCol + 128, acol + 32 + kk * 8, bdesc, idesc, acc);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(dcol, acol + kk * 8, sdesc_k_sw128(bsm + kk * 32), idesc, (c | kk) != 0);
           mma_commit(&ctl.empty[s]);
           mma_commit(&ctl.a_empty[sa]);
         }
         if (!ok) break;
-        mma_commit(&ctl.d_full);
+        mma_commit(&ctl.d_full[db]);
         ++nu;
       }
       // every issued MMA must retire before tensor memory is released
       mma_commit(&ctl.drain);
-      mbar_wait(&ctl.drain, 0, &ctl.zero, a.timeout_ns);
+      mbar_wait(&ctl.drain, 0, &ctl.zero, lim);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------- dequantisation + epilogue
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int h = warp >> 2;          // pass 0: gate (0) / up (1) matrix; pass 1: K half
-    const int r = q * 32 + lane;      // A row = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-
-    if (MODE == 0 && a.y_acc != nullptr) {
-      // zero the fp32 combine buffer for the down pass that follows on the stream
-      const size_t n4 = static_cast<size_t>(a.T) * a.d / 4;
-      float4* y4 = reinterpret_cast<float4*>(a.y_acc);
-      const size_t step = static_cast<size_t>(gridDim.x) * (kDqWarps * 32);
-      for (size_t i = static_cast<size_t>(blockIdx.x) * (kDqWarps * 32) + tid; i < n4; i += step)
-        y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-
-    uint32_t it = 0, ita = 0, nu = 0;
+  } else if (warp < kDqWarps) {
+    // ------------------------------------------------------ dequantisation
+    const int q = warp & 3;           // TMEM lane quarter
+    const int par = warp >> 2;        // K-chunk parity served by this warp
+    const int L = q * 32 + lane;      // TMEM lane = A row
+    const int srow = lane_to_srow<MODE>(L);
+    const uint32_t taddr_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int sw = (srow >> 2) & 1;   // 32B swizzle: the two 16-byte halves swap on bit 2 of the row
+    uint32_t it = 0, ita = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
-      if (!decode_unit<MODE>(a, n_rt, u, U)) continue;
-      const int npad = (U.rows + 15) & ~15;
+      if (!decode_unit(a, n_rt, u, U)) continue;
       int r0, r1;
       a_rows<MODE>(a, U, r0, r1);
       const int ng = U.K / 64;
-      const int wrow = (MODE == 0) ? (h == 0 ? r0 : r1) + r : r0 + r;
+      const int wrow = srow < 64 ? r0 + srow : r1 + (srow - 64);
       const uint16_t* sp = (U.shared ? a.sh_scale : a.scale) + static_cast<size_t>(wrow) * ng;
       const uint16_t* bp = (U.shared ? a.sh_bias : a.bias) + static_cast<size_t>(wrow) * ng;
-      const int srow = (MODE == 0) ? h * 128 + r : r;   // packed row in the smem stage
+      uint16_t s_next = 0, b_next = 0;
+      if (par < ng) {
+        s_next = __ldg(sp + par);
+        b_next = __ldg(bp + par);
+      }
       for (int c = 0; c < ng; ++c, ++it, ++ita) {
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1u;
-        const int sa = ita % C::kAStages;
-        const uint32_t pha = (ita / C::kAStages) & 1u;
-        const uint32_t s2 = bf16_pair(__ldg(sp + c));
-        const uint32_t b2 = bf16_pair(__ldg(bp + c));
-        if (!__all_sync(kFull, mbar_wait(&ctl.full[s], ph, abortp, a.timeout_ns))) {
+        if ((c & 1) != par) continue;
+        const uint32_t s2 = bf16_pair(s_next), b2 = bf16_pair(b_next);
+        if (c + 2 < ng) {             // prefetch this warp's next group
+          s_next = __ldg(sp + c + 2);
+          b_next = __ldg(bp + c + 2);
+        }
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        const int sa = ita % kAStages;
+        const uint32_t pha = (ita / kAStages) & 1u;
+        if (!__all_sync(kFull, mbar_wait(&ctl.full[s], ph, abortp, lim))) {
           if (lane == 0) raise_abort(ctl, a.err);
           ok = false;
           break;
         }
-        // packed row: 32 bytes, two 16-byte halves swapped when bit 2 of the row is set
-        const uint8_t* rowp = sA + s * L::kABytes + srow * 32;
-        const int sw = (srow >> 2) & 1;
-        uint4 w0, w1;
-        if (MODE == 0) {
-          w0 = *reinterpret_cast<const uint4*>(rowp + 16 * (0 ^ sw));
-          w1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 ^ sw));
-        } else {
-          w0 = *reinterpret_cast<const uint4*>(rowp + 16 * (h ^ sw));
-          w1 = w0;
-        }
+        const uint8_t* rowp = sA + s * kABytes + srow * 32;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(rowp + 16 * sw);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 - sw));
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
-        if (!__all_sync(kFull, mbar_wait(&ctl.a_empty[sa], pha ^ 1u, abortp, a.timeout_ns))) {
+        if (!__all_sync(kFull, mbar_wait(&ctl.a_empty[sa], pha ^ 1u, abortp, lim))) {
           if (lane == 0) raise_abort(ctl, a.err);
           ok = false;
           break;
@@ -377,84 +383,147 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         dequant8(w0.y, s2, b2, v + 4);
         dequant8(w0.z, s2, b2, v + 8);
         dequant8(w0.w, s2, b2, v + 12);
-        if (MODE == 0) {
-          const uint32_t col = sa * C::kACols + h * 32;
-          tmem_st_32x32b_x16(tmem + lane_base + col, v);
-          dequant8(w1.x, s2, b2, v + 0);
-          dequant8(w1.y, s2, b2, v + 4);
-          dequant8(w1.z, s2, b2, v + 8);
-          dequant8(w1.w, s2, b2, v + 12);
-          tmem_st_32x32b_x16(tmem + lane_base + col + 16, v);
-        } else {
-          tmem_st_32x32b_x16(tmem + lane_base + sa * C::kACols + h * 16, v);
-        }
+        tmem_st_32x32b_x16(taddr_lane + sa * kACols, v);
+        dequant8(w1.x, s2, b2, v + 0);
+        dequant8(w1.y, s2, b2, v + 4);
+        dequant8(w1.z, s2, b2, v + 8);
+        dequant8(w1.w, s2, b2, v + 12);
+        tmem_st_32x32b_x16(taddr_lane + sa * kACols + 16, v);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.a_full[sa]);
       }
-      if (!ok) break;
-
-      // ---------------------------------------------------------- epilogue
-      if (!__all_sync(kFull, mbar_wait(&ctl.d_full, nu & 1u, abortp, a.timeout_ns))) {
+    }
+  } else if (warp < kEpiWarp0 + kEpiWarps) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp - kEpiWarp0;
+    const int et = q * 32 + lane;     // 0..127
+    const uint32_t taddr_q = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t gs_phase = 0;
+    if (MODE == 0 && a.y_acc != nullptr) {
+      // zero the fp32 combine buffer for the down pass that follows on the stream
+      const size_t n4 = static_cast<size_t>(a.T) * a.d / 4;
+      float4* y4 = reinterpret_cast<float4*>(a.y_acc);
+      const size_t step = static_cast<size_t>(gridDim.x) * (kEpiWarps * 32);
+      for (size_t i = static_cast<size_t>(blockIdx.x) * (kEpiWarps * 32) + et; i < n4; i += step)
+        y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint32_t nu = 0, nchunk = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      Unit U;
+      if (!decode_unit(a, n_rt, u, U)) continue;
+      const int npad = (U.rows + 15) & ~15;
+      const uint32_t db = nu & 1u;
+      const uint32_t dcol = kDCol + db * 128;
+      if (MODE == 1) {
+        // token and weight of each row of the tile (shared expert: weight 1)
+        int tt = -1;
+        float wv = 0.f;
+        if (et < U.rows) {
+          if (U.shared) {
+            tt = U.row0 + et;
+            wv = 1.f;
+          } else {
+            const int p = __ldg(a.perm + U.row0 + et);
+            tt = p / a.k;
+            wv = __ldg(a.wts + p);
+          }
+        }
+        ctl.e_tok[db][et] = tt;
+        ctl.e_w[db][et] = wv;
+      } else {
+        // the previous unit's act tile stores must have finished reading the staging tile
+        if (q == 0) bulk_wait_read<0>();
+      }
+      if (!epi_sync(ctl, gs_phase, lim)) {
+        if (lane == 0) raise_abort(ctl, a.err);
+        break;
+      }
+      if (!__all_sync(kFull, mbar_wait(&ctl.d_full[db], (nu >> 1) & 1u, abortp, lim))) {
         if (lane == 0) raise_abort(ctl, a.err);
         break;
       }
       tc_fence_after();
       if (MODE == 0) {
-        const int F = U.shared ? a.f_s : a.f;
-        uint16_t* out = (U.shared ? a.act_sh : a.act) + static_cast<size_t>(U.row0) * F +
-                        U.fb * 128 + r;
-        for (int cc = h; cc * 32 < npad; cc += 2) {
-          uint32_t g[32], up[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + kDCol + cc * 32, g);
-          tmem_ld_32x32b_x32(tmem + lane_base + kDCol + 128 + cc * 32, up);
-          tmem_ld_wait();
+        // lanes 32q..32q+15 hold features 16q..16q+7 (gate, then up 8 lanes later),
+        // lanes 32q+16.. hold features 16q+8..16q+15
+        const int t4 = lane >> 2, tc = 2 * (lane & 3);
+        for (int cc = 0; cc * 32 < npad; ++cc) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = cc * 32 + j;
-            if (col < U.rows) {
-              const float gv = __uint_as_float(g[j]);
-              const float uv = __uint_as_float(up[j]);
-              const __nv_bfloat16 act = __float2bfloat16_rn(silu_f(gv) * uv);
-              out[static_cast<size_t>(col) * F] = __bfloat16_as_ushort(act);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[16];
+            tmem_ld_16x256b_x4(taddr_q + (static_cast<uint32_t>(half * 16) << 16) + dcol + cc * 32, r);
+            tmem_ld_wait();
+            const int fl = 16 * q + 8 * half + t4;          // local feature 0..63
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const int tok = cc * 32 + 8 * j + tc + e2;   // row within the tile
+                const float g = __uint_as_float(r[4 * j + e2]);
+                const float up = __uint_as_float(r[4 * j + 2 + e2]);
+                const uint32_t off = tok * 128 + ((((fl * 2) >> 4) ^ (tok & 7)) << 4) + ((fl * 2) & 15);
+                *reinterpret_cast<uint16_t*>(sEpi + off) = bf16_bits(silu_f(g) * up);
+              }
             }
           }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.d_empty[db]);
+        fence_proxy_async_smem();
+        if (!epi_sync(ctl, gs_phase, lim)) {
+          if (lane == 0) raise_abort(ctl, a.err);
+          break;
+        }
+        if (q == 0) {
+          const CUtensorMap* mC = U.shared ? &tmC_sh : &tmC;
+          for (int g = lane; g < npad / 16; g += 32)
+            tma_store_2d(mC, sEpi + g * 2048, U.fb * 64, U.act0 + 16 * g);
+          bulk_commit();
         }
       } else {
-        const int feat = U.fb * 128 + r;
-        for (int cc = h; cc * 32 < npad; cc += 2) {
+        const int feat = U.fb * 128 + q * 32 + lane;
+        for (int cc = 0; cc * 32 < npad; ++cc, ++nchunk) {
           uint32_t dv[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + kDCol + cc * 32, dv);
+          tmem_ld_32x32b_x32(taddr_q + dcol + cc * 32, dv);
           tmem_ld_wait();
-          const int col = cc * 32 + lane;
-          int tt = -1;
-          float wv = 0.f;
-          if (col < U.rows) {
-            if (U.shared) {
-              tt = U.row0 + col;
-              wv = 1.f;
-            } else {
-              const int p = __ldg(a.perm + U.row0 + col);
-              tt = p / a.k;
-              wv = __ldg(a.wts + p);
-            }
+          float* st = reinterpret_cast<float*>(sEpi + (nchunk & 1u) * 16384);
+          // the reduce that last read this staging buffer must be done with it
+          if (q == 0) bulk_wait_read<1>();
+          if (!epi_sync(ctl, gs_phase, lim)) {
+            ok = false;
+            break;
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tj = __shfl_sync(kFull, tt, j);
-            const float wj = __shfl_sync(kFull, wv, j);
-            if (tj >= 0)
-              atomicAdd(a.y_acc + static_cast<size_t>(tj) * a.d + feat,
-                        wj * __uint_as_float(dv[j]));
+          for (int j = 0; j < 32; ++j)
+            st[j * 128 + q * 32 + lane] = __uint_as_float(dv[j]) * ctl.e_w[db][cc * 32 + j];
+          fence_proxy_async_smem();
+          if (!epi_sync(ctl, gs_phase, lim)) {
+            ok = false;
+            break;
+          }
+          if (q == 0) {
+            const int tj = ctl.e_tok[db][min(cc * 32 + lane, kNMax - 1)];
+            if (cc * 32 + lane < U.rows && tj >= 0)
+              bulk_reduce_add_f32(a.y_acc + static_cast<size_t>(tj) * a.d + feat - lane,
+                                  st + lane * 128, 512);
+            bulk_commit();
           }
         }
+        if (!ok) {
+          if (lane == 0) raise_abort(ctl, a.err);
+          break;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.d_empty[db]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.d_empty);
       ++nu;
     }
+    if (q == 0) bulk_wait<0>();   // outstanding stores / reductions complete before exit
   }
 
   __syncthreads();
@@ -485,19 +554,17 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
 }
 
 template <int MODE>
-cudaError_t launch_mode(const GemmArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmA_sh,
-                        const CUtensorMap& tmB, const CUtensorMap& tmB_sh, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s) {
   static bool attr_set = false;   // per process; the attribute is per function
-  constexpr size_t smem = smem_bytes<MODE>();
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(q4_grouped_gemm_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  q4_grouped_gemm_kernel<MODE><<<grid, kGemmThreads, smem, s>>>(tmA, tmA_sh, tmB, tmB_sh, a);
+  q4_grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(m.A, m.A_sh, m.B, m.B_sh, m.C,
+                                                                   m.C_sh, a);
   return cudaGetLastError();
 }
 
@@ -505,25 +572,30 @@ cudaError_t launch_mode(const GemmArgs& a, const CUtensorMap& tmA, const CUtenso
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s) {
+int act_rows_capacity(int T, int k, int max_tiles) {
+  return T * k + 16 * max_tiles + kNMax;
+}
+
+FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles) {
   FfnWs w{};
   size_t o = 0;
-  w.act = o;     o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(T) * k * f, 256);
-  w.act_sh = o;  o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(T) * f_s, 256);
-  w.y_acc = o;   o = align_up(o + sizeof(float) * static_cast<size_t>(T) * d, 256);
+  w.act = o;
+  o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(act_rows_capacity(T, k, max_tiles)) * f, 256);
+  w.act_sh = o;
+  o = align_up(o + sizeof(uint16_t) * align_up(static_cast<size_t>(T), kNMax) * f_s, 256);
+  w.y_acc = o;
+  o = align_up(o + sizeof(float) * static_cast<size_t>(T) * d, 256);
   w.total = o;
   return w;
 }
 
-int gemm_tile_rows(int mode) { return mode == 0 ? Cfg<0>::kNMax : Cfg<1>::kNMax; }
+int gemm_tile_rows() { return kNMax; }
 
-size_t gemm_smem_bytes() { return smem_bytes<0>() > smem_bytes<1>() ? smem_bytes<0>() : smem_bytes<1>(); }
+size_t gemm_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_gemm(int mode, const GemmArgs& a, const CUtensorMap& tmA,
-                        const CUtensorMap& tmA_sh, const CUtensorMap& tmB,
-                        const CUtensorMap& tmB_sh, int grid, cudaStream_t s) {
-  if (mode == 0) return launch_mode<0>(a, tmA, tmA_sh, tmB, tmB_sh, grid, s);
-  return launch_mode<1>(a, tmA, tmA_sh, tmB, tmB_sh, grid, s);
+cudaError_t launch_gemm(int mode, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s) {
+  if (mode == 0) return launch_mode<0>(a, m, grid, s);
+  return launch_mode<1>(a, m, grid, s);
 }
 
 cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStream_t s) {

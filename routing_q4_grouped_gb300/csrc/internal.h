@@ -53,7 +53,7 @@ void stage_mark(int i, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM
 
-constexpr int kGemmThreads = 320;          // 8 dequant/epilogue warps, producer, MMA
+constexpr int kGemmThreads = 448;          // 8 dequant, 4 epilogue, producer, MMA warps
 
 struct GemmArgs {
   int K;                    // reduction length of routed units (d: gate/up, f: down)
@@ -66,31 +66,40 @@ struct GemmArgs {
   const float* wts;         // [T*k] routing weights
   int n_fb;                 // feature blocks per routed tile
   int n_fb_sh;              // feature blocks per shared tile
-  int n_sh_tiles;           // shared tiles (gemm_tile_rows(mode) rows each)
+  int n_sh_tiles;           // shared tiles (gemm_tile_rows() rows each)
   const uint16_t* scale;    // routed scale/bias of the packed A matrix
   const uint16_t* bias;
   const uint16_t* sh_scale; // shared-expert scale/bias
   const uint16_t* sh_bias;
-  uint16_t* act;            // [T*k][f]  (gate/up output, down input)
-  uint16_t* act_sh;         // [T][f_s]
-  float* y_acc;             // [T][d]
+  float* y_acc;             // [T][d] fp32 combine buffer (zeroed by pass 0)
   int32_t* err;
   uint64_t timeout_ns;
 };
 
+// TMA descriptors of one pass: packed A (routed, shared), token rows B (routed,
+// shared), activation store C (routed, shared; pass 0 only).
+struct GemmMaps {
+  CUtensorMap A, A_sh, B, B_sh, C, C_sh;
+};
+
+// Activation rows of routed tile `ti` (first permuted row `row0`) start at a
+// 16-aligned row; tiles never overlap even when padded to 16 rows.
+__host__ __device__ inline int act_tile_base(int row0, int ti) {
+  return (row0 + 16 * ti + 15) & ~15;
+}
+int act_rows_capacity(int T, int k, int max_tiles);
+
 struct FfnWs {
   size_t act, act_sh, y_acc, total;
 };
-FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s);
+FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles);
 
 // mode 0: gate/up + SwiGLU -> act (also zeroes y_acc); mode 1: down + weighted combine -> y_acc
-cudaError_t launch_gemm(int mode, const GemmArgs& a, const CUtensorMap& tmA,
-                        const CUtensorMap& tmA_sh, const CUtensorMap& tmB,
-                        const CUtensorMap& tmB_sh, int grid, cudaStream_t s);
+cudaError_t launch_gemm(int mode, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s);
 
 cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStream_t s);
 
 size_t gemm_smem_bytes();
-int gemm_tile_rows(int mode);   // max rows per unit: 128 (gate/up pass), 256 (down pass)
+int gemm_tile_rows();   // max rows per unit and rows per shared-expert tile (128)
 
 }  // namespace moeq4

@@ -56,8 +56,8 @@ _lib = None
 _SIGS = {
     "moe_route_max_tiles": (_c_i32, [_c_i32, _c_i32, _c_i32, _c_i32]),
     "moe_route_workspace_size": (_c_size, [_c_i32, _c_i32, _c_i32]),
-    "moe_ffn_workspace_size": (_c_size, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32]),
-    "moe_layer_workspace_size": (_c_size, [_c_i32] * 6),
+    "moe_ffn_workspace_size": (_c_size, [_c_i32] * 7),
+    "moe_layer_workspace_size": (_c_size, [_c_i32] * 7),
     "moe_route": (_c_i32, [_c_ptr, ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
     "moe_expert_ffn": (_c_i32, [_c_ptr, _c_i32, _c_i32, ctypes.POINTER(Q4WeightsC),
                                 ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
@@ -69,6 +69,7 @@ _SIGS = {
     "moe_debug_dequant": (_c_i32, [_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr, _c_ptr]),
     "moe_debug_mma": (_c_i32, [_c_i32, _c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr]),
     "moe_debug_set_stage_events": (_c_i32, [ctypes.POINTER(_c_ptr), _c_i32]),
+    "moe_debug_tmem_layout": (_c_i32, [_c_ptr, _c_ptr]),
 }
 
 
@@ -115,12 +116,12 @@ def moe_route_workspace_size(T, E, k) -> int:
     return lib().moe_route_workspace_size(T, E, k)
 
 
-def moe_ffn_workspace_size(T, k, d, f, f_s) -> int:
-    return lib().moe_ffn_workspace_size(T, k, d, f, f_s)
+def moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m=128) -> int:
+    return lib().moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m)
 
 
-def moe_layer_workspace_size(T, E, k, d, f, f_s) -> int:
-    return lib().moe_layer_workspace_size(T, E, k, d, f, f_s)
+def moe_layer_workspace_size(T, E, k, d, f, f_s, block_m=128) -> int:
+    return lib().moe_layer_workspace_size(T, E, k, d, f, f_s, block_m)
 
 
 # ------------------------------------------------------------------ device buffers
@@ -259,6 +260,10 @@ def moe_debug_mma(a_from_tmem: bool, A, B, D, stream=None) -> None:
                                                 _stream(stream)))
 
 
+def moe_debug_tmem_layout(out, stream=None) -> None:
+    _check("moe_debug_tmem_layout", lib().moe_debug_tmem_layout(_ptr(out), _stream(stream)))
+
+
 def moe_debug_set_stage_events(events) -> None:
     """Registers torch.cuda.Event objects recorded at the layer's stage boundaries."""
     arr = (_c_ptr * max(1, len(events)))(*[e.cuda_event for e in events])
@@ -271,7 +276,7 @@ class Layer:
     def __init__(self, W: DeviceWeights, T: int, k: int, block_m: int = 128, device="cuda"):
         self.W, self.T, self.k = W, T, k
         self.route = RouteBuffers.alloc(T, W.E, k, block_m, device)
-        self.ws = alloc_workspace(moe_layer_workspace_size(T, W.E, k, W.d, W.f, W.f_s), device)
+        self.ws = alloc_workspace(moe_layer_workspace_size(T, W.E, k, W.d, W.f, W.f_s, block_m), device)
         self.y = torch.empty((T, W.d), dtype=torch.bfloat16, device=device)
 
     def __call__(self, x, logits, stream=None):

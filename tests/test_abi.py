@@ -33,7 +33,7 @@ def test_headers_declare_the_boundary():
     for n in ("moe_route", "moe_expert_ffn", "moe_layer", "moe_route_max_tiles",
               "moe_route_workspace_size", "moe_ffn_workspace_size", "moe_layer_workspace_size",
               "moe_get_device_error", "moe_status_string", "moe_residual_rms", "moe_debug_dequant", "moe_debug_mma",
-              "moe_debug_set_stage_events"):
+              "moe_debug_set_stage_events", "moe_debug_tmem_layout"):
         assert n in names, n
 
 
@@ -47,9 +47,9 @@ def test_host_side_sizes(L):
     assert L.moe_route_max_tiles(4096, 256, 8, 128) == 4096 * 8 // 128 + 256
     assert L.moe_route_max_tiles(3, 4, 2, 2) == 3 + 4
     assert L.moe_route_workspace_size(4096, 256, 8) > 4096 * 8 * 4
-    ffn = L.moe_ffn_workspace_size(4096, 8, 2048, 512, 512)
+    ffn = L.moe_ffn_workspace_size(4096, 256, 8, 2048, 512, 512, 128)
     assert ffn >= 4096 * 8 * 512 * 2 + 4096 * 512 * 2 + 4096 * 2048 * 4
-    lay = L.moe_layer_workspace_size(4096, 256, 8, 2048, 512, 512)
+    lay = L.moe_layer_workspace_size(4096, 256, 8, 2048, 512, 512, 128)
     assert lay >= ffn + L.moe_route_workspace_size(4096, 256, 8)
     assert L.status_string(0) == "ok"
     assert "workspace" in L.status_string(-3)

@@ -66,3 +66,23 @@ def test_dequant_hand_groups():
     got = _dequant_gpu(qw, s, b)
     assert np.array_equal(got, O.to_bf16(O.dequant(qw, s, b)))
     assert np.array_equal(O.bf16_value(got[0]), codes[0].astype(np.float64))
+
+
+def test_tmem_16x256b_fragment_layout():
+    """Thread t of warp q, repetition j: registers 4j, 4j+1 hold lane base + t/4 at
+    columns 8j + 2(t%4) + {0, 1}; registers 4j+2, 4j+3 hold lane base + 8 + t/4."""
+    out = torch.zeros((128, 32), dtype=torch.int32, device="cuda")
+    moeq4.moe_debug_tmem_layout(out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    want = np.zeros((128, 32), dtype=np.int64)
+    for q in range(4):
+        for t in range(32):
+            for half in range(2):
+                base = 32 * q + 16 * half
+                for j in range(4):
+                    for r in range(4):
+                        lane = base + t // 4 + (8 if r >= 2 else 0)
+                        col = 8 * j + 2 * (t % 4) + (r & 1)
+                        want[32 * q + t, 16 * half + 4 * j + r] = (lane << 16) | col
+    assert np.array_equal(got, want)
