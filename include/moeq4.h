@@ -22,7 +22,7 @@
  *    that ran out of time) set bits in the caller's device error word and
  *    never trap; read it with moe_get_device_error after synchronising.
  *  - Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), 1 <= block_m <= 128,
- *    T*k < 2^30, d % 128 == 0, f % 128 == 0, f_s % 128 == 0, d <= 16384,
+ *    T*k < 2^30, d % 256 == 0, f % 128 == 0, f_s % 128 == 0, d <= 16384,
  *    f, f_s <= 8192.
  */
 #ifndef MOEQ4_H
@@ -77,6 +77,33 @@ typedef struct moe_q4_weights {
   moe_q4_mat sh_down;
   int32_t E, d, f, f_s;
 } moe_q4_weights;
+
+/* The same weights in the kernel-native order that moe_expert_ffn streams,
+ * produced once by moe_q4_prepack (values unchanged; only their order differs).
+ * Each matrix [R][K] is cut into units of 256 rows (two 128-row tiles) and
+ * K-chunks of 64; chunk c of unit u is one contiguous 9216-byte block:
+ *   bytes [0, 8192)     codes of tile 0 then tile 1: 128 rows x 32 bytes, the
+ *                       row's two 16-byte halves swapped when bit 2 of the row
+ *                       index is set, nibbles of each word in the order
+ *                       k0 k2 k4 k6 k1 k3 k5 k7
+ *   bytes [8192, 9216)  2 x 128 words: scale | bias << 16 (bf16 bits)
+ * Row i of tile t of unit p of expert e is, for gate/up (F = f or f_s),
+ *   e*2F + up*F + 64*(2p + t) + 8*(i >> 4) + (i & 7), up = (i >> 3) & 1
+ * (gate and up rows of a feature interleaved in blocks of 8), and for down
+ *   e*d + 256p + 128t + i.
+ * Matrices follow each other: routed gate/up, routed down, shared gate/up,
+ * shared down. */
+typedef struct moe_q4_packed {
+  const void* data;   /* device buffer of moe_q4_packed_size() bytes */
+  int32_t E, d, f, f_s;
+} moe_q4_packed;
+
+/* Bytes of the kernel-native copy of one layer's weights (same as the inputs). */
+size_t moe_q4_packed_size(int32_t E, int32_t d, int32_t f, int32_t f_s);
+
+/* Reorders W into the kernel-native layout at dst (device, dst_bytes >=
+ * moe_q4_packed_size). Run once when the weights are loaded. */
+moe_status moe_q4_prepack(const moe_q4_weights* W, void* dst, size_t dst_bytes, void* stream);
 
 /* Routing result, written by moe_route, read by moe_expert_ffn. Device arrays:
  *   ids     int32 [T][k]   chosen experts per token, descending logit, ties to lower index
@@ -141,18 +168,18 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  *   y[t] = bf16( sum_j w[t,j] * FFN_{ids[t,j]}(x[t]) + FFN_shared(x[t]) ),
  *   FFN_e(x) = Wd_e * bf16( silu(Wg_e x) * (Wu_e x) ).
  *   x   bf16 [T][d] token activations (device)
- *   W   layer weights (host struct, device arrays), W->d must equal d
+ *   W   layer weights in the kernel-native layout (moe_q4_prepack); W->d must equal d
  *   r   routing result of moe_route for the same T (device arrays)
  *   y   bf16 [T][d] output (device)
  *   ws  scratch of moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m) bytes */
-moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weights* W,
+moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed* W,
                           const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream);
 
 /* moe_route followed by moe_expert_ffn on the same stream, no host sync.
  *   x bf16 [T][d], logits fp32 [T][E]; r receives the routing result; y bf16 [T][d].
  *   ws of moe_layer_workspace_size(...) bytes, zero-filled before first use. */
-moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_weights* W,
+moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_packed* W,
                      const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                      void* stream);
 

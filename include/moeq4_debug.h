@@ -17,7 +17,8 @@ extern "C" {
 #endif
 
 /* Expands a 4-bit groupwise-affine matrix to bf16 in global memory with the
- * same register routine the grouped GEMM uses ("Perplexity Lily 오픈소스 공개 …",
+ * same routines the grouped GEMM uses (the kernel-native nibble order of the
+ * prepack, then the register dequantisation; "Perplexity Lily 오픈소스 공개 …",
  * §5-1 format; value bf16(scale*q + bias) rounded once).
  *   qw [rows][K/8] uint32, scale/bias [rows][K/64] bf16  ->  out [rows][K] bf16.
  * K % 64 == 0. The product path never materialises this array. */

@@ -111,16 +111,29 @@ moe_status check_mat(const moe_q4_mat& m) {
   return MOE_OK;
 }
 
+moe_status check_dims(int E, int d, int f, int f_s) {
+  if (E < 1 || E > 1024 || d < 1 || f < 1 || f_s < 0) return MOE_ERR_ARG;
+  if (d % 256 || f % 128 || f_s % 128 || d > 16384 || f > 8192 || f_s > 8192) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
 moe_status check_weights(const moe_q4_weights* W) {
   if (!W) return MOE_ERR_ARG;
-  if (W->E < 1 || W->E > 1024 || W->d < 1 || W->f < 1 || W->f_s < 0) return MOE_ERR_ARG;
-  if (W->d % 128 || W->f % 128 || W->f_s % 128 || W->d > 16384 || W->f > 8192 || W->f_s > 8192)
-    return MOE_ERR_SHAPE;
-  moe_status s;
+  moe_status s = check_dims(W->E, W->d, W->f, W->f_s);
+  if (s != MOE_OK) return s;
   if ((s = check_mat(W->gate_up)) != MOE_OK || (s = check_mat(W->down)) != MOE_OK) return s;
   if (W->f_s > 0 &&
       ((s = check_mat(W->sh_gate_up)) != MOE_OK || (s = check_mat(W->sh_down)) != MOE_OK))
     return s;
+  return MOE_OK;
+}
+
+moe_status check_packed(const moe_q4_packed* W) {
+  if (!W) return MOE_ERR_ARG;
+  moe_status s = check_dims(W->E, W->d, W->f, W->f_s);
+  if (s != MOE_OK) return s;
+  if (!W->data) return MOE_ERR_ARG;
+  if (!aligned16(W->data)) return MOE_ERR_ALIGN;
   return MOE_OK;
 }
 
@@ -169,15 +182,17 @@ moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, siz
   return MOE_OK;
 }
 
-moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weights* W,
+moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed* W,
                     const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                     cudaStream_t s) {
   moe_status st = check_route_out(r);
   if (st != MOE_OK) return st;
-  if ((st = check_weights(W)) != MOE_OK) return st;
+  if ((st = check_packed(W)) != MOE_OK) return st;
   if (!x || !y || !ws) return MOE_ERR_ARG;
   if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_ALIGN;
   if (T != r->T || d != W->d || W->E != r->E) return MOE_ERR_SHAPE;
+  const PackLayout P = pack_layout(W->E, W->d, W->f, W->f_s);
+  const uint8_t* pk = static_cast<const uint8_t*>(W->data);
   const int k = r->k, E = W->E, f = W->f, fs = W->f_s;
   const int max_tiles = moe_route_max_tiles(T, E, k, r->block_m);
   const FfnWs L = ffn_ws_layout(T, k, d, f, fs, max_tiles);
@@ -209,8 +224,7 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weight
   a.timeout_ns = timeout_ns();
   const int n_sh_tiles = fs ? (T + gemm_tile_rows() - 1) / gemm_tile_rows() : 0;
 
-  const CUtensorMapSwizzle SW32 = CU_TENSOR_MAP_SWIZZLE_32B, SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
-  const CUtensorMapDataType U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+  const CUtensorMapSwizzle SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
   // ---- pass 0: gate/up + SwiGLU
@@ -219,24 +233,15 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weight
     GemmMaps m;
     g.K = d;
     g.K_sh = d;
-    g.n_fb = f / 64;
-    g.n_fb_sh = fs / 64;
+    g.n_fb = P.gu.units;
+    g.n_fb_sh = P.sgu.units;
     g.n_sh_tiles = n_sh_tiles;
-    g.scale = W->gate_up.scale;
-    g.bias = W->gate_up.bias;
-    g.sh_scale = fs ? W->sh_gate_up.scale : W->gate_up.scale;
-    g.sh_bias = fs ? W->sh_gate_up.bias : W->gate_up.bias;
-    bool ok = encode_2d(&m.A, U32, 4, W->gate_up.qw, d / 8, static_cast<uint64_t>(E) * 2 * f, 8,
-                        64, SW32) &&
-              encode_2d(&m.B, BF16, 2, x, d, T, 64, 1, SW128) &&
+    g.pk = pk + P.gu.offset;
+    g.pk_sh = pk + P.sgu.offset;
+    bool ok = encode_2d(&m.B, BF16, 2, x, d, T, 64, 1, SW128) &&
               encode_2d(&m.C, BF16, 2, act, f, act_rows, 64, 16, SW128);
-    if (fs)
-      ok = ok && encode_2d(&m.A_sh, U32, 4, W->sh_gate_up.qw, d / 8, 2ull * fs, 8, 64, SW32) &&
-           encode_2d(&m.C_sh, BF16, 2, act_sh, fs, act_sh_rows, 64, 16, SW128);
-    else {
-      m.A_sh = m.A;
-      m.C_sh = m.C;
-    }
+    if (fs) ok = ok && encode_2d(&m.C_sh, BF16, 2, act_sh, fs, act_sh_rows, 64, 16, SW128);
+    else m.C_sh = m.C;
     m.B_sh = m.B;
     if (!ok) return MOE_ERR_CUDA;
     if (launch_gemm(0, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -248,23 +253,14 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weight
     GemmMaps m;
     g.K = f;
     g.K_sh = fs;
-    g.n_fb = d / 128;
-    g.n_fb_sh = fs ? d / 128 : 0;
+    g.n_fb = P.dn.units;
+    g.n_fb_sh = P.sdn.units;
     g.n_sh_tiles = n_sh_tiles;
-    g.scale = W->down.scale;
-    g.bias = W->down.bias;
-    g.sh_scale = fs ? W->sh_down.scale : W->down.scale;
-    g.sh_bias = fs ? W->sh_down.bias : W->down.bias;
-    bool ok = encode_2d(&m.A, U32, 4, W->down.qw, f / 8, static_cast<uint64_t>(E) * d, 8, 64,
-                        SW32) &&
-              encode_2d(&m.B, BF16, 2, act, f, act_rows, 64, 16, SW128);
-    if (fs)
-      ok = ok && encode_2d(&m.A_sh, U32, 4, W->sh_down.qw, fs / 8, d, 8, 64, SW32) &&
-           encode_2d(&m.B_sh, BF16, 2, act_sh, fs, act_sh_rows, 64, 16, SW128);
-    else {
-      m.A_sh = m.A;
-      m.B_sh = m.B;
-    }
+    g.pk = pk + P.dn.offset;
+    g.pk_sh = pk + P.sdn.offset;
+    bool ok = encode_2d(&m.B, BF16, 2, act, f, act_rows, 64, 16, SW128);
+    if (fs) ok = ok && encode_2d(&m.B_sh, BF16, 2, act_sh, fs, act_sh_rows, 64, 16, SW128);
+    else m.B_sh = m.B;
     m.C = m.B;
     m.C_sh = m.B_sh;
     if (!ok) return MOE_ERR_CUDA;
@@ -323,18 +319,49 @@ size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int3
   return align256(a) + b;
 }
 
+size_t moe_q4_packed_size(int32_t E, int32_t d, int32_t f, int32_t f_s) {
+  if (check_dims(E, d, f, f_s) != MOE_OK) return 0;
+  return pack_layout(E, d, f, f_s).total;
+}
+
+moe_status moe_q4_prepack(const moe_q4_weights* W, void* dst, size_t dst_bytes, void* stream) {
+  moe_status st = check_weights(W);
+  if (st != MOE_OK) return st;
+  if (!dst) return MOE_ERR_ARG;
+  if (!aligned16(dst)) return MOE_ERR_ALIGN;
+  const PackLayout P = pack_layout(W->E, W->d, W->f, W->f_s);
+  if (dst_bytes < P.total) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* o = static_cast<uint8_t*>(dst);
+  const int E = W->E, d = W->d, f = W->f, fs = W->f_s;
+  if (launch_prepack(W->gate_up.qw, W->gate_up.scale, W->gate_up.bias, E, 2 * f, d, 0, f,
+                     o + P.gu.offset, s) != cudaSuccess ||
+      launch_prepack(W->down.qw, W->down.scale, W->down.bias, E, d, f, 1, d, o + P.dn.offset,
+                     s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (fs > 0 &&
+      (launch_prepack(W->sh_gate_up.qw, W->sh_gate_up.scale, W->sh_gate_up.bias, 1, 2 * fs, d, 0,
+                      fs, o + P.sgu.offset, s) != cudaSuccess ||
+       launch_prepack(W->sh_down.qw, W->sh_down.scale, W->sh_down.bias, 1, d, fs, 1, d,
+                      o + P.sdn.offset, s) != cudaSuccess))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, size_t ws_bytes,
                      void* stream) {
   return route_impl(logits, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_weights* W,
+moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed* W,
                           const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream) {
   return ffn_impl(x, T, d, W, r, y, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_weights* W,
+moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_packed* W,
                      const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                      void* stream) {
   if (!W || !r) return MOE_ERR_ARG;
@@ -344,7 +371,7 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
   const size_t rsz = align256(moe_route_workspace_size(T, r->E, r->k));
   moe_status st;
   // validate the FFN arguments before anything is enqueued
-  if ((st = check_weights(W)) != MOE_OK) return st;
+  if ((st = check_packed(W)) != MOE_OK) return st;
   if (!x || !y) return MOE_ERR_ARG;
   if (W->E != r->E) return MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(256) dequant_probe_kernel(const uint32_t* __re
     const size_t row = i / wpr, w = i % wpr;
     const size_t g = row * (K / 64) + w / 8;
     uint32_t v[4];
-    dequant8(qw[i], bf16_pair(scale[g]), bf16_pair(bias[g]), v);
+    dequant8(permute_nibbles(qw[i]), bf16_pair(scale[g]), bf16_pair(bias[g]), v);
     reinterpret_cast<uint4*>(out)[i] = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }

@@ -5,33 +5,39 @@
 // Lily, Qwen 추론 최적화" (aitrends.kr), section "Qwen 구조와 Prefill 경로").
 //
 // Orientation (weights on the MMA's M side): D[features, tokens] = W[features, K]
-// * X[tokens, K]^T, M = 128 weight rows, N = the tile's rows padded to 16 (<= 128),
-// K in chunks of 64 = one quantisation group. Dequantised weights go from
-// registers into tensor memory (tcgen05.st) and feed the MMA as operand A, so no
-// bf16 weight tile touches shared or global memory. Token rows arrive by TMA:
-// gather4 of x rows for the gate/up pass, 16-row tiles of the (tile-padded)
-// activation rows for the down pass.
+// * X[tokens, K]^T with M = 128 weight rows per A tile, N = the tile's rows padded
+// to 16 (<= 128) and K in chunks of 64 = one quantisation group. A unit is one
+// block-map tile times 256 weight rows = two A tiles, so every token-row chunk in
+// shared memory feeds two MMAs. Dequantised weights go from registers straight
+// into tensor memory (tcgen05.st) as the MMA's A operand: no bf16 weight tile
+// touches shared or global memory.
 //
-// Warp roles (448 threads, one CTA per SM, persistent over units):
-//   warps 0-7   dequantisation; warp w serves TMEM lane quarter w%4 and the
-//               K-chunks of parity w/4 of every unit
-//   warps 8-11  epilogue (lane quarter w-8), overlapped with the next unit's
-//               mainloop through two accumulator buffers
-//   warp 12     TMA producer (packed codes + token rows into a 6-stage ring)
-//   warp 13     TMEM allocator and single-thread MMA issuer
-// Tensor memory: columns [0, 256) hold 8 A stages of 32 columns (128 rows x 64
-// bf16), [256, 512) two 128-column fp32 accumulators.
+// Data movement (TMA instructions cost the issuing warp tens of cycles each, so
+// the bytes per instruction and the number of issuing warps set the rate):
+//   packed weights  one 9 KB bulk copy per K-chunk (kernel-native layout)
+//   token rows      gate/up pass: gather4 of x rows; down pass: 16-row tiles of
+//                   the tile-padded activation rows; issued by six warps
 //
-// Pass 0 (gate/up): a unit covers 64 output features; its A tile interleaves
-//   the gate and up rows in blocks of 8 (TMEM lanes 16m..16m+7 = gate features
-//   8m.., lanes 16m+8.. = the matching up features), so one 16x256b tensor-memory
-//   load gives each epilogue thread gate and up values of the same feature and
-//   token: act = bf16(silu(gate) * up), staged in shared memory and written with
-//   TMA tile stores. This pass also zeroes the fp32 combine buffer.
-// Pass 1 (down): a unit covers 128 output features of the tile's rows; the
-//   epilogue scales each token column by its routing weight (1 for the shared
-//   expert) and adds the 512-byte row slices into y_acc with asynchronous bulk
-//   reduce-add copies.
+// Warp roles (608 threads, one CTA per SM, persistent over units):
+//   warps 0-7    dequantisation: warp w fills A tile w/4, TMEM lane quarter w%4
+//   warps 8-11   epilogue, lane quarter w-8
+//   warps 12-17  producers
+//   warp 18      TMEM allocator and single-thread MMA issuer
+// Tensor memory: columns [0, 256) hold 4 A stages of 64 columns (two tiles of
+// 128 rows x 64 bf16), [256, 512) the two accumulators (A tile j -> 256 + 128 j).
+// An accumulator is released as soon as the epilogue has read it, so the next
+// unit's MMAs on tile 0 overlap the epilogue of tile 1.
+//
+// Pass 0 (gate/up): A tile j covers 64 output features with gate and up rows
+//   interleaved in blocks of 8 (TMEM lanes 16m..16m+7 = gate rows of features
+//   8m.., lanes 16m+8.. = their up rows); one 16x256b tensor-memory load gives an
+//   epilogue thread gate and up values of one feature and two tokens:
+//   act = bf16(silu(gate) * up), staged in shared memory, written by TMA tile
+//   stores into the tile-padded activation rows. This pass zeroes y_acc.
+// Pass 1 (down): A tile j covers 128 output features; the epilogue scales token
+//   columns by their routing weight (1 for the shared expert), turns each warp's
+//   32 x 32 block around in shared memory and adds it into y_acc with 16-byte
+//   vector reductions (red.global.add.v4.f32).
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -47,24 +53,25 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kNMax = 128;                 // rows per unit (MMA N)
 constexpr int kStages = 6;                 // shared-memory ring depth
-constexpr int kAStages = 8;                // TMEM A stages
-constexpr int kACols = 32;                 // TMEM columns per A stage
+constexpr int kAStages = 4;                // TMEM A stages
+constexpr int kACols = 64;                 // TMEM columns per A stage (two tiles x 32)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = 256;            // accumulator buffer b at column 256 + 128 b
+constexpr uint32_t kDCol = 256;            // accumulator of tile j at column 256 + 128 j
 constexpr int kDqWarps = 8;
 constexpr int kEpiWarp0 = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kProdWarp0 = 12;
+constexpr int kProdWarps = 6;
+constexpr int kMmaWarp = 18;
+constexpr int kThreads = 19 * 32;
 static_assert(kThreads == kGemmThreads, "thread count");
 
 constexpr int kBBytes = kNMax * 128;       // token rows: 64 bf16 (128 B) each, 128B swizzle
-constexpr int kABytes = 128 * 32;          // packed codes: 64 codes (32 B) per row, 32B swizzle
-constexpr int kEpiBytes = 32768;           // pass 0: act tile [128][64] bf16; pass 1: 2 x [32][128] fp32
+constexpr int kABytes = kPackChunkBytes;   // one packed K-chunk of the unit
+constexpr int kEpiBytes = 32768;           // pass 0: 2 act tiles [128][64] bf16; pass 1: 4 x [32][32] fp32
 constexpr size_t kOffB = 0;
 constexpr size_t kOffA = kOffB + size_t(kStages) * kBBytes;
-constexpr size_t kOffEpi = kOffA + size_t(kStages) * kABytes;
+constexpr size_t kOffEpi = (kOffA + size_t(kStages) * kABytes + 1023) / 1024 * 1024;
 constexpr size_t kOffCtl = kOffEpi + kEpiBytes;
 
 struct Ctl {
@@ -72,32 +79,31 @@ struct Ctl {
   uint64_t empty[kStages];
   uint64_t a_full[kAStages];
   uint64_t a_empty[kAStages];
-  uint64_t d_full[2];
+  uint64_t d_full;
   uint64_t d_empty[2];
   uint64_t epi_bar;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int zero;
-  int tok[kNMax];      // producer: x rows to gather (pass 0)
-  int e_tok[2][kNMax];    // epilogue: token of each row (pass 1), -1 = padding; per unit parity
-  float e_w[2][kNMax];    // epilogue: routing weight of each row (pass 1)
+  int e_tok[2][kNMax];    // epilogue (pass 1): token of each row, -1 = padding; by unit parity
+  float e_w[2][kNMax];    // epilogue (pass 1): routing weight of each row
 };
 
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Ctl);
 
 struct Unit {
-  int e, row0, rows, fb, K;
+  int e, row0, rows, p, K;
   int act0;    // first activation row of the tile (16-aligned, tile-padded layout)
   bool shared;
 };
 
-// Unit u -> (tile, feature block). Routed units first, tile-major, then shared.
+// Unit u -> (tile, unit column p). Routed units first, tile-major, then shared.
 __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, Unit& U) {
   const int n_routed = n_rt * a.n_fb;
   if (u < n_routed) {
     const int ti = u / a.n_fb;
-    U.fb = u - ti * a.n_fb;
+    U.p = u - ti * a.n_fb;
     const int32_t* tl = a.tiles + 3 * static_cast<size_t>(ti);
     U.e = __ldg(tl);
     U.row0 = __ldg(tl + 1);
@@ -111,7 +117,7 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
   } else {
     const int v = u - n_routed;
     const int st = v / a.n_fb_sh;
-    U.fb = v - st * a.n_fb_sh;
+    U.p = v - st * a.n_fb_sh;
     U.e = 0;
     U.row0 = st * kNMax;
     U.rows = min(kNMax, a.T - U.row0);
@@ -122,24 +128,11 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
   return true;
 }
 
-// First packed-matrix rows of the unit's two 64-row halves of A.
-template <int MODE>
-__device__ __forceinline__ void a_rows(const GemmArgs& a, const Unit& U, int& r0, int& r1) {
-  if (MODE == 0) {
-    const int F = U.shared ? a.f_s : a.f;
-    r0 = U.e * 2 * F + U.fb * 64;   // gate rows
-    r1 = r0 + F;                    // the matching up rows
-  } else {
-    r0 = U.e * a.d + U.fb * 128;
-    r1 = r0 + 64;
-  }
-}
-
-// TMEM lane L of the unit's A tile -> row of the packed shared-memory tile.
-template <int MODE>
-__device__ __forceinline__ int lane_to_srow(int L) {
-  if (MODE == 0) return ((L >> 3) & 1) * 64 + 8 * (L >> 4) + (L & 7);
-  return L;
+// First byte of the unit's packed blocks (chunk c at + c * kPackChunkBytes).
+__device__ __forceinline__ const uint8_t* unit_blocks(const GemmArgs& a, const Unit& U) {
+  const uint8_t* base = U.shared ? a.pk_sh : a.pk;
+  const int units = U.shared ? a.n_fb_sh : a.n_fb;
+  return base + (static_cast<size_t>(U.e) * units + U.p) * (U.K / 64) * kPackChunkBytes;
 }
 
 __device__ __forceinline__ void raise_abort(Ctl& ctl, int32_t* err) {
@@ -161,11 +154,18 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    q4_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmA_sh,
-                           const __grid_constant__ CUtensorMap tmB,
+    q4_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB_sh,
                            const __grid_constant__ CUtensorMap tmC,
                            const __grid_constant__ CUtensorMap tmC_sh, const GemmArgs a) {
@@ -181,16 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], kDqWarps / 2 + 1);
+      mbar_init(&ctl.empty[s], kDqWarps + 1);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&ctl.a_full[s], kDqWarps / 2);
+      mbar_init(&ctl.a_full[s], kDqWarps);
       mbar_init(&ctl.a_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&ctl.d_full[b], 1);
-      mbar_init(&ctl.d_empty[b], kEpiWarps);
-    }
+    mbar_init(&ctl.d_full, 1);
+    mbar_init(&ctl.d_empty[0], kEpiWarps);
+    mbar_init(&ctl.d_empty[1], kEpiWarps);
     mbar_init(&ctl.epi_bar, kEpiWarps);
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
@@ -201,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmA_sh);
+  if (warp == kProdWarp0 && lane == 0) {
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmB_sh);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmC_sh);
   }
   tc_fence_before();
   __syncthreads();
@@ -221,28 +220,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int total = n_rt * a.n_fb + a.n_sh_tiles * a.n_fb_sh;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    const uint64_t pol_x = policy_evict_last();   // token rows: reused by every feature block
+  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
+    // ------------------------------------------------------------- producers
+    const int pw = warp - kProdWarp0;
+    const uint64_t pol_x = policy_evict_last();   // token rows: reused by every unit of a tile
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
       if (!decode_unit(a, n_rt, u, U)) {
-        if (lane == 0) atomicOr(a.err, MOE_DEVERR_BAD_TILE);
+        if (pw == 0 && lane == 0) atomicOr(a.err, MOE_DEVERR_BAD_TILE);
         continue;
       }
       const int npad = (U.rows + 15) & ~15;
-      const CUtensorMap* mA = U.shared ? &tmA_sh : &tmA;
+      const uint8_t* blocks = unit_blocks(a, U);
       const CUtensorMap* mB = U.shared ? &tmB_sh : &tmB;
-      int r0, r1;
-      a_rows<MODE>(a, U, r0, r1);
-      if (MODE == 0) {
-        for (int i = lane; i < npad; i += 32) {
-          const int r = min(i, U.rows - 1);
-          ctl.tok[i] = U.shared ? U.row0 + r : __ldg(a.perm + U.row0 + r) / a.k;
+      // this lane's token-row copy for every chunk of the unit (at most one)
+      const int nops = MODE == 0 ? npad / 4 : npad / 16;
+      const int g = kProdWarps * lane + pw;
+      const bool has_op = g < nops;
+      int r4[4] = {0, 0, 0, 0};
+      if (has_op) {
+        if (MODE == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = min(4 * g + i, U.rows - 1);
+            r4[i] = U.shared ? U.row0 + idx : __ldg(a.perm + U.row0 + idx) / a.k;
+          }
+        } else {
+          r4[0] = U.act0 + 16 * g;
         }
-        __syncwarp();
       }
       const uint32_t bytes = kABytes + npad * 128;
       const int nch = U.K / 64;
@@ -254,25 +261,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* dA = sA + s * kABytes;
-        uint8_t* dB = sB + s * kBBytes;
-        if (lane == 0) {
+        if (pw == 0 && lane == 0) {
           mbar_arrive_expect_tx(&ctl.full[s], bytes);
-          tma_load_2d(dA, mA, &ctl.full[s], c * 8, r0, 0);
-          tma_load_2d(dA + 64 * 32, mA, &ctl.full[s], c * 8, r1, 0);
+          bulk_load(sA + s * kABytes, blocks + static_cast<size_t>(c) * kABytes, kABytes,
+                    &ctl.full[s]);
         }
-        __syncwarp();
-        if (MODE == 0) {
-          for (int g = lane; g < npad / 4; g += 32)
-            tma_gather4(dB + g * 512, mB, &ctl.full[s], c * 64, ctl.tok[4 * g],
-                        ctl.tok[4 * g + 1], ctl.tok[4 * g + 2], ctl.tok[4 * g + 3], pol_x);
-        } else {
-          for (int g = lane; g < npad / 16; g += 32)
-            tma_load_2d(dB + g * 2048, mB, &ctl.full[s], c * 64, U.act0 + 16 * g, pol_x);
+        if (has_op) {
+          uint8_t* dB = sB + s * kBBytes;
+          if (MODE == 0)
+            tma_gather4(dB + g * 512, mB, &ctl.full[s], c * 64, r4[0], r4[1], r4[2], r4[3], pol_x);
+          else
+            tma_load_2d(dB + g * 2048, mB, &ctl.full[s], c * 64, r4[0], pol_x);
         }
       }
     }
-    if (!ok && lane == 0) {
+    if (!ok && pw == 0 && lane == 0) {
       // let copies already in flight land before the CTA's shared memory goes away
       const uint32_t n = it < static_cast<uint32_t>(kStages) ? it : kStages;
       for (uint32_t i = 1; i <= n; ++i) {
@@ -290,15 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!decode_unit(a, n_rt, u, U)) continue;
         const uint32_t npad = (U.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(128, npad);
-        const uint32_t db = nu & 1u;
-        if (!mbar_wait(&ctl.d_empty[db], ((nu >> 1) & 1u) ^ 1u, abortp, lim)) {
-          raise_abort(ctl, a.err);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t dcol = tmem + kDCol + db * 128;
         const int nch = U.K / 64;
-        for (int c = 0; c < nch; ++c, ++it, ++ita) {
+        for (int c = 0; c < nch && ok; ++c, ++it, ++ita) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           const int sa = ita % kAStages;
@@ -311,15 +307,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t bsm = smem_u32(sB + s * kBBytes);
-          const uint32_t acol = tmem + sa * kACols;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(dcol, acol + kk * 8, sdesc_k_sw128(bsm + kk * 32), idesc, (c | kk) != 0);
+          for (int j = 0; j < 2; ++j) {
+            if (c == 0) {   // the epilogue must have drained this accumulator
+              if (!mbar_wait(&ctl.d_empty[j], (nu & 1u) ^ 1u, abortp, lim)) {
+                raise_abort(ctl, a.err);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t dcol = tmem + kDCol + 128 * j;
+            const uint32_t acol = tmem + sa * kACols + 32 * j;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(dcol, acol + kk * 8, sdesc_k_sw128(bsm + kk * 32), idesc, (c | kk) != 0);
+          }
+          if (!ok) break;
           mma_commit(&ctl.empty[s]);
           mma_commit(&ctl.a_empty[sa]);
         }
         if (!ok) break;
-        mma_commit(&ctl.d_full[db]);
+        mma_commit(&ctl.d_full);
         ++nu;
       }
       // every issued MMA must retire before tensor memory is released
@@ -330,34 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kDqWarps) {
     // ------------------------------------------------------ dequantisation
     const int q = warp & 3;           // TMEM lane quarter
-    const int par = warp >> 2;        // K-chunk parity served by this warp
+    const int j = warp >> 2;          // A tile filled by this warp
     const int L = q * 32 + lane;      // TMEM lane = A row
-    const int srow = lane_to_srow<MODE>(L);
-    const uint32_t taddr_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int sw = (srow >> 2) & 1;   // 32B swizzle: the two 16-byte halves swap on bit 2 of the row
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j;
+    const int sw = (L >> 2) & 1;      // the row's 16-byte halves are stored swapped when set
     uint32_t it = 0, ita = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
       if (!decode_unit(a, n_rt, u, U)) continue;
-      int r0, r1;
-      a_rows<MODE>(a, U, r0, r1);
-      const int ng = U.K / 64;
-      const int wrow = srow < 64 ? r0 + srow : r1 + (srow - 64);
-      const uint16_t* sp = (U.shared ? a.sh_scale : a.scale) + static_cast<size_t>(wrow) * ng;
-      const uint16_t* bp = (U.shared ? a.sh_bias : a.bias) + static_cast<size_t>(wrow) * ng;
-      uint16_t s_next = 0, b_next = 0;
-      if (par < ng) {
-        s_next = __ldg(sp + par);
-        b_next = __ldg(bp + par);
-      }
-      for (int c = 0; c < ng; ++c, ++it, ++ita) {
-        if ((c & 1) != par) continue;
-        const uint32_t s2 = bf16_pair(s_next), b2 = bf16_pair(b_next);
-        if (c + 2 < ng) {             // prefetch this warp's next group
-          s_next = __ldg(sp + c + 2);
-          b_next = __ldg(bp + c + 2);
-        }
+      const int nch = U.K / 64;
+      for (int c = 0; c < nch; ++c, ++it, ++ita) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         const int sa = ita % kAStages;
@@ -367,9 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint8_t* rowp = sA + s * kABytes + srow * 32;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(rowp + 16 * sw);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 - sw));
+        const uint8_t* blk = sA + s * kABytes;
+        const uint8_t* rowp = blk + j * 4096 + L * 32;
+        const uint4 h0 = *reinterpret_cast<const uint4*>(rowp + 16 * sw);
+        const uint4 h1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 - sw));
+        const uint32_t sbw = reinterpret_cast<const uint32_t*>(blk + 8192)[j * 128 + L];
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);
         if (!__all_sync(kFull, mbar_wait(&ctl.a_empty[sa], pha ^ 1u, abortp, lim))) {
@@ -378,17 +372,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        const uint32_t s2 = bf16_pair(static_cast<uint16_t>(sbw & 0xFFFFu));
+        const uint32_t b2 = bf16_pair(static_cast<uint16_t>(sbw >> 16));
         uint32_t v[16];
-        dequant8(w0.x, s2, b2, v + 0);
-        dequant8(w0.y, s2, b2, v + 4);
-        dequant8(w0.z, s2, b2, v + 8);
-        dequant8(w0.w, s2, b2, v + 12);
-        tmem_st_32x32b_x16(taddr_lane + sa * kACols, v);
-        dequant8(w1.x, s2, b2, v + 0);
-        dequant8(w1.y, s2, b2, v + 4);
-        dequant8(w1.z, s2, b2, v + 8);
-        dequant8(w1.w, s2, b2, v + 12);
-        tmem_st_32x32b_x16(taddr_lane + sa * kACols + 16, v);
+        dequant8(h0.x, s2, b2, v + 0);
+        dequant8(h0.y, s2, b2, v + 4);
+        dequant8(h0.z, s2, b2, v + 8);
+        dequant8(h0.w, s2, b2, v + 12);
+        tmem_st_32x32b_x16(taddr + sa * kACols, v);
+        dequant8(h1.x, s2, b2, v + 0);
+        dequant8(h1.y, s2, b2, v + 4);
+        dequant8(h1.z, s2, b2, v + 8);
+        dequant8(h1.w, s2, b2, v + 12);
+        tmem_st_32x32b_x16(taddr + sa * kACols + 16, v);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -409,14 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (size_t i = static_cast<size_t>(blockIdx.x) * (kEpiWarps * 32) + et; i < n4; i += step)
         y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    uint32_t nu = 0, nchunk = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+    uint32_t nu = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       Unit U;
       if (!decode_unit(a, n_rt, u, U)) continue;
       const int npad = (U.rows + 15) & ~15;
       const uint32_t db = nu & 1u;
-      const uint32_t dcol = kDCol + db * 128;
       if (MODE == 1) {
         // token and weight of each row of the tile (shared expert: weight 1)
         int tt = -1;
@@ -426,53 +420,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             tt = U.row0 + et;
             wv = 1.f;
           } else {
-            const int p = __ldg(a.perm + U.row0 + et);
-            tt = p / a.k;
-            wv = __ldg(a.wts + p);
+            const int pr = __ldg(a.perm + U.row0 + et);
+            tt = pr / a.k;
+            wv = __ldg(a.wts + pr);
           }
         }
         ctl.e_tok[db][et] = tt;
         ctl.e_w[db][et] = wv;
       } else {
-        // the previous unit's act tile stores must have finished reading the staging tile
+        // the previous unit's activation stores must have finished reading the staging tiles
         if (q == 0) bulk_wait_read<0>();
       }
-      if (!epi_sync(ctl, gs_phase, lim)) {
-        if (lane == 0) raise_abort(ctl, a.err);
-        break;
-      }
-      if (!__all_sync(kFull, mbar_wait(&ctl.d_full[db], (nu >> 1) & 1u, abortp, lim))) {
+      if (!epi_sync(ctl, gs_phase, lim) ||
+          !__all_sync(kFull, mbar_wait(&ctl.d_full, nu & 1u, abortp, lim))) {
         if (lane == 0) raise_abort(ctl, a.err);
         break;
       }
       tc_fence_after();
       if (MODE == 0) {
-        // lanes 32q..32q+15 hold features 16q..16q+7 (gate, then up 8 lanes later),
-        // lanes 32q+16.. hold features 16q+8..16q+15
+        // lanes 32q..32q+15 hold features 16q..16q+7 of the tile (gate, then up 8 lanes
+        // later), lanes 32q+16.. features 16q+8..16q+15
         const int t4 = lane >> 2, tc = 2 * (lane & 3);
-        for (int cc = 0; cc * 32 < npad; ++cc) {
+        for (int jt = 0; jt < 2; ++jt) {
+          uint8_t* stile = sEpi + jt * 16384;
+          for (int cc = 0; cc * 32 < npad; ++cc) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t r[16];
-            tmem_ld_16x256b_x4(taddr_q + (static_cast<uint32_t>(half * 16) << 16) + dcol + cc * 32, r);
-            tmem_ld_wait();
-            const int fl = 16 * q + 8 * half + t4;          // local feature 0..63
+            for (int half = 0; half < 2; ++half) {
+              uint32_t r[16];
+              tmem_ld_16x256b_x4(taddr_q + (static_cast<uint32_t>(half * 16) << 16) + kDCol +
+                                     128 * jt + cc * 32,
+                                 r);
+              tmem_ld_wait();
+              const int fl = 16 * q + 8 * half + t4;          // feature within the tile
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+              for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
-              for (int e2 = 0; e2 < 2; ++e2) {
-                const int tok = cc * 32 + 8 * j + tc + e2;   // row within the tile
-                const float g = __uint_as_float(r[4 * j + e2]);
-                const float up = __uint_as_float(r[4 * j + 2 + e2]);
-                const uint32_t off = tok * 128 + ((((fl * 2) >> 4) ^ (tok & 7)) << 4) + ((fl * 2) & 15);
-                *reinterpret_cast<uint16_t*>(sEpi + off) = bf16_bits(silu_f(g) * up);
+                for (int e2 = 0; e2 < 2; ++e2) {
+                  const int tok = cc * 32 + 8 * jj + tc + e2;  // row within the tile
+                  const float g = __uint_as_float(r[4 * jj + e2]);
+                  const float up = __uint_as_float(r[4 * jj + 2 + e2]);
+                  const uint32_t off =
+                      tok * 128 + ((((fl * 2) >> 4) ^ (tok & 7)) << 4) + ((fl * 2) & 15);
+                  *reinterpret_cast<uint16_t*>(stile + off) = bf16_bits(silu_f(g) * up);
+                }
               }
             }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.d_empty[jt]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.d_empty[db]);
         fence_proxy_async_smem();
         if (!epi_sync(ctl, gs_phase, lim)) {
           if (lane == 0) raise_abort(ctl, a.err);
@@ -480,46 +477,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (q == 0) {
           const CUtensorMap* mC = U.shared ? &tmC_sh : &tmC;
-          for (int g = lane; g < npad / 16; g += 32)
-            tma_store_2d(mC, sEpi + g * 2048, U.fb * 64, U.act0 + 16 * g);
+          const int per = npad / 16;
+          if (lane < 2 * per) {
+            const int jt = lane / per, g = lane - jt * per;
+            tma_store_2d(mC, sEpi + jt * 16384 + g * 2048, (2 * U.p + jt) * 64, U.act0 + 16 * g);
+          }
           bulk_commit();
         }
       } else {
-        const int feat = U.fb * 128 + q * 32 + lane;
-        for (int cc = 0; cc * 32 < npad; ++cc, ++nchunk) {
-          uint32_t dv[32];
-          tmem_ld_32x32b_x32(taddr_q + dcol + cc * 32, dv);
-          tmem_ld_wait();
-          float* st = reinterpret_cast<float*>(sEpi + (nchunk & 1u) * 16384);
-          // the reduce that last read this staging buffer must be done with it
-          if (q == 0) bulk_wait_read<1>();
-          if (!epi_sync(ctl, gs_phase, lim)) {
-            ok = false;
-            break;
-          }
+        // warp-private transpose through shared memory: lane = output feature in
+        // TMEM, then lane = 4 consecutive features of one token for a 16-byte reduction
+        float* st = reinterpret_cast<float*>(sEpi) + q * 32 * 32;
+        const int rsub = lane >> 3, c4 = 4 * (lane & 7);
+        for (int jt = 0; jt < 2; ++jt) {
+          const int col0 = 256 * U.p + 128 * jt + 32 * q;   // this warp's first output feature
+          for (int cc = 0; cc * 32 < npad; ++cc) {
+            uint32_t dv[32];
+            tmem_ld_32x32b_x32(taddr_q + kDCol + 128 * jt + cc * 32, dv);
+            tmem_ld_wait();
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            st[j * 128 + q * 32 + lane] = __uint_as_float(dv[j]) * ctl.e_w[db][cc * 32 + j];
-          fence_proxy_async_smem();
-          if (!epi_sync(ctl, gs_phase, lim)) {
-            ok = false;
-            break;
+            for (int jj = 0; jj < 32; ++jj)
+              st[jj * 32 + lane] = __uint_as_float(dv[jj]) * ctl.e_w[db][cc * 32 + jj];
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int row = 4 * i + rsub;                 // token column within the chunk
+              const int tj = ctl.e_tok[db][cc * 32 + row];
+              if (cc * 32 + row < U.rows && tj >= 0) {
+                const float4 v = *reinterpret_cast<const float4*>(st + row * 32 + c4);
+                red_add_v4_f32(a.y_acc + static_cast<size_t>(tj) * a.d + col0 + c4, v.x, v.y, v.z,
+                               v.w);
+              }
+            }
           }
-          if (q == 0) {
-            const int tj = ctl.e_tok[db][min(cc * 32 + lane, kNMax - 1)];
-            if (cc * 32 + lane < U.rows && tj >= 0)
-              bulk_reduce_add_f32(a.y_acc + static_cast<size_t>(tj) * a.d + feat - lane,
-                                  st + lane * 128, 512);
-            bulk_commit();
-          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.d_empty[jt]);
         }
-        if (!ok) {
-          if (lane == 0) raise_abort(ctl, a.err);
-          break;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.d_empty[db]);
       }
       ++nu;
     }
@@ -563,8 +558,7 @@ cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& m, int grid, cudaStre
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  q4_grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(m.A, m.A_sh, m.B, m.B_sh, m.C,
-                                                                   m.C_sh, a);
+  q4_grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(m.B, m.B_sh, m.C, m.C_sh, a);
   return cudaGetLastError();
 }
 

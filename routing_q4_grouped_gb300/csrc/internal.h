@@ -51,9 +51,49 @@ cudaError_t launch_route_scatter(const RouteArgs& a, cudaStream_t s);  // kernel
 // Optional stage events (bench/test timing): mark(i) records event i on `s`.
 void stage_mark(int i, cudaStream_t s);
 
+// ------------------------------------------------- kernel-native weight layout
+//
+// A matrix [R][K] (R weight rows, K reduction) is cut into units of 256 rows,
+// two 128-row A tiles whose row order is the TMEM lane order the GEMM uses, and
+// K-chunks of 64 (one quantisation group). Chunk c of unit u is one contiguous
+// block of kPackChunkBytes: the codes of tile 0 then tile 1 (128 rows x 32 B each;
+// the two 16-byte halves of row L swapped when bit 2 of L is set; nibbles of each
+// word in the order k0 k2 k4 k6 k1 k3 k5 k7), then 2 x 128 words (scale | bias << 16).
+// Blocks are ordered unit-major, chunk-minor.
+constexpr int kPackChunkBytes = 2 * 128 * 32 + 2 * 128 * 4;   // 9216
+
+struct PackedMat {
+  size_t offset;      // byte offset of the matrix in the packed buffer
+  int units;          // units per expert
+  int K;              // reduction length
+  int experts;
+};
+struct PackLayout {
+  PackedMat gu, dn, sgu, sdn;   // routed gate/up, routed down, shared gate/up, shared down
+  size_t total;
+};
+PackLayout pack_layout(int E, int d, int f, int f_s);
+
+// Packed-matrix row of lane L of A tile j of unit p of expert e.
+// Gate/up (F = f or f_s): the unit covers output features [128p, 128p + 128),
+// tile j their 64-feature block 2p + j, with lanes 16m..16m+7 = gate rows of
+// features 8m.. and lanes 16m+8.. = the matching up rows.
+__host__ __device__ inline int pack_row_gate_up(int e, int F, int p, int j, int L) {
+  const int m = L >> 4, up = (L >> 3) & 1, i = L & 7;
+  return e * 2 * F + up * F + 64 * (2 * p + j) + 8 * m + i;
+}
+// Down: the unit covers output features [256p, 256p + 256), tile j half j.
+__host__ __device__ inline int pack_row_down(int e, int d, int p, int j, int L) {
+  return e * d + 256 * p + 128 * j + L;
+}
+
+cudaError_t launch_prepack(const uint32_t* qw, const uint16_t* scale, const uint16_t* bias,
+                           int experts, int R, int K, int kind, int F_or_d, uint8_t* dst,
+                           cudaStream_t s);   // kind 0: gate/up, 1: down
+
 // ------------------------------------------------------------ grouped GEMM
 
-constexpr int kGemmThreads = 448;          // 8 dequant, 4 epilogue, producer, MMA warps
+constexpr int kGemmThreads = 608;          // 8 dequant, 4 epilogue, 6 producer, 1 MMA warps
 
 struct GemmArgs {
   int K;                    // reduction length of routed units (d: gate/up, f: down)
@@ -64,22 +104,20 @@ struct GemmArgs {
   int max_tiles;            // capacity of the block map (bounds check)
   const int32_t* perm;      // [T*k]
   const float* wts;         // [T*k] routing weights
-  int n_fb;                 // feature blocks per routed tile
-  int n_fb_sh;              // feature blocks per shared tile
+  int n_fb;                 // units (256 weight rows) per routed tile
+  int n_fb_sh;              // units per shared tile
   int n_sh_tiles;           // shared tiles (gemm_tile_rows() rows each)
-  const uint16_t* scale;    // routed scale/bias of the packed A matrix
-  const uint16_t* bias;
-  const uint16_t* sh_scale; // shared-expert scale/bias
-  const uint16_t* sh_bias;
+  const uint8_t* pk;        // packed routed matrix of this pass
+  const uint8_t* pk_sh;     // packed shared-expert matrix of this pass
   float* y_acc;             // [T][d] fp32 combine buffer (zeroed by pass 0)
   int32_t* err;
   uint64_t timeout_ns;
 };
 
-// TMA descriptors of one pass: packed A (routed, shared), token rows B (routed,
-// shared), activation store C (routed, shared; pass 0 only).
+// TMA descriptors of one pass: token rows B (routed, shared) and the activation
+// store C (routed, shared; pass 0 only).
 struct GemmMaps {
-  CUtensorMap A, A_sh, B, B_sh, C, C_sh;
+  CUtensorMap B, B_sh, C, C_sh;
 };
 
 // Activation rows of routed tile `ti` (first permuted row `row0`) start at a

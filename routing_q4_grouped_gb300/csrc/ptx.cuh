@@ -123,6 +123,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src,
       : "memory");
 }
 
+// global[dst .. dst+16) += {a, b, c, d} (fp32, relaxed, GPU scope), no return value.
+__device__ __forceinline__ void red_add_v4_f32(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

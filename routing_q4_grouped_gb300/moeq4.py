@@ -38,6 +38,10 @@ class Q4WeightsC(ctypes.Structure):
                 ("E", _c_i32), ("d", _c_i32), ("f", _c_i32), ("f_s", _c_i32)]
 
 
+class Q4PackedC(ctypes.Structure):
+    _fields_ = [("data", _c_ptr), ("E", _c_i32), ("d", _c_i32), ("f", _c_i32), ("f_s", _c_i32)]
+
+
 class RouteOutC(ctypes.Structure):
     _fields_ = [("ids", _c_ptr), ("w", _c_ptr), ("counts", _c_ptr), ("offsets", _c_ptr),
                 ("perm", _c_ptr), ("inv", _c_ptr), ("tiles", _c_ptr), ("n_tiles", _c_ptr),
@@ -59,9 +63,11 @@ _SIGS = {
     "moe_ffn_workspace_size": (_c_size, [_c_i32] * 7),
     "moe_layer_workspace_size": (_c_size, [_c_i32] * 7),
     "moe_route": (_c_i32, [_c_ptr, ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
-    "moe_expert_ffn": (_c_i32, [_c_ptr, _c_i32, _c_i32, ctypes.POINTER(Q4WeightsC),
+    "moe_q4_packed_size": (_c_size, [_c_i32] * 4),
+    "moe_q4_prepack": (_c_i32, [ctypes.POINTER(Q4WeightsC), _c_ptr, _c_size, _c_ptr]),
+    "moe_expert_ffn": (_c_i32, [_c_ptr, _c_i32, _c_i32, ctypes.POINTER(Q4PackedC),
                                 ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
-    "moe_layer": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4WeightsC),
+    "moe_layer": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4PackedC),
                            ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "moe_get_device_error": (_c_i32, [_c_ptr, ctypes.POINTER(_c_i32), _c_ptr]),
     "moe_status_string": (ctypes.c_char_p, [_c_i32]),
@@ -126,18 +132,32 @@ def moe_layer_workspace_size(T, E, k, d, f, f_s, block_m=128) -> int:
 
 # ------------------------------------------------------------------ device buffers
 
+def moe_q4_packed_size(E, d, f, f_s) -> int:
+    return lib().moe_q4_packed_size(E, d, f, f_s)
+
+
+def moe_q4_prepack(W: "DeviceWeights", dst: torch.Tensor, stream=None) -> None:
+    """Reorders the interchange-layout device weights of W into dst (kernel-native)."""
+    wc = W.interchange_cstruct()
+    _check("moe_q4_prepack", lib().moe_q4_prepack(ctypes.byref(wc), _ptr(dst), dst.numel(),
+                                                  _stream(stream)))
+
+
 @dataclasses.dataclass
 class DeviceWeights:
-    """One layer's packed weights resident on the GPU (torch tensors as storage)."""
+    """One layer's 4-bit weights on the GPU: the kernel-native copy the layer
+    streams (``packed``) and, until :meth:`drop_interchange`, the interchange
+    arrays it was made from (torch tensors as storage)."""
     E: int
     d: int
     f: int
     f_s: int
     tensors: dict
+    packed: torch.Tensor = None
 
     @classmethod
-    def from_host(cls, W, device="cuda"):
-        """Copies a :class:`routing_q4_grouped_gb300.synth.Q4Weights` to the device."""
+    def from_host(cls, W, device="cuda", keep_interchange=False):
+        """Copies a :class:`routing_q4_grouped_gb300.synth.Q4Weights` to the device and prepacks it."""
         names = ["gu_qw", "gu_scale", "gu_bias", "dn_qw", "dn_scale", "dn_bias"]
         if W.f_s:
             names += ["sgu_qw", "sgu_scale", "sgu_bias", "sdn_qw", "sdn_scale", "sdn_bias"]
@@ -146,17 +166,29 @@ class DeviceWeights:
             a = getattr(W, n)
             t = torch.from_numpy(a.view(a.dtype.str.replace("u", "i")) if a.dtype.kind == "u" else a)
             ts[n] = t.to(device)
-        return cls(W.E, W.d, W.f, W.f_s, ts)
+        dw = cls(W.E, W.d, W.f, W.f_s, ts)
+        dw.packed = torch.empty(moe_q4_packed_size(W.E, W.d, W.f, W.f_s), dtype=torch.uint8,
+                                device=device)
+        moe_q4_prepack(dw, dw.packed)
+        if not keep_interchange:
+            torch.cuda.current_stream().synchronize()
+            dw.tensors = {}
+        return dw
 
-    def cstruct(self) -> Q4WeightsC:
+    def interchange_cstruct(self) -> Q4WeightsC:
         t = self.tensors
+        if not t:
+            raise RuntimeError("interchange arrays were dropped after prepacking")
         m = lambda p: Q4Mat(_ptr(t.get(p + "_qw")), _ptr(t.get(p + "_scale")), _ptr(t.get(p + "_bias")))
         return Q4WeightsC(m("gu"), m("dn"), m("sgu") if self.f_s else Q4Mat(),
                           m("sdn") if self.f_s else Q4Mat(), self.E, self.d, self.f, self.f_s)
 
+    def cstruct(self) -> Q4PackedC:
+        return Q4PackedC(_ptr(self.packed), self.E, self.d, self.f, self.f_s)
+
     @property
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in self.tensors.values())
+        return self.packed.numel()
 
 
 @dataclasses.dataclass

@@ -32,7 +32,8 @@ def test_headers_declare_the_boundary():
     names = _declared()
     for n in ("moe_route", "moe_expert_ffn", "moe_layer", "moe_route_max_tiles",
               "moe_route_workspace_size", "moe_ffn_workspace_size", "moe_layer_workspace_size",
-              "moe_get_device_error", "moe_status_string", "moe_residual_rms", "moe_debug_dequant", "moe_debug_mma",
+              "moe_get_device_error", "moe_status_string", "moe_residual_rms",
+              "moe_q4_packed_size", "moe_q4_prepack", "moe_debug_dequant", "moe_debug_mma",
               "moe_debug_set_stage_events", "moe_debug_tmem_layout"):
         assert n in names, n
 
@@ -70,12 +71,21 @@ def test_bad_arguments_rejected_on_host(L):
     r.block_m = 128
     assert lib.moe_route(fake, ctypes.byref(r), fake, 0, None) == -3      # workspace too small
     assert lib.moe_route(fake + 4, ctypes.byref(r), fake, 1 << 30, None) == -7   # misaligned
+    P = L.Q4PackedC(fake, 8, 200, 128, 0)   # d not a multiple of 256
+    assert lib.moe_expert_ffn(fake, 16, 200, ctypes.byref(P), ctypes.byref(r), fake, fake,
+                              1 << 30, None) == -2
+    P = L.Q4PackedC(None, 8, 256, 128, 0)   # no weight buffer
+    assert lib.moe_expert_ffn(fake, 16, 256, ctypes.byref(P), ctypes.byref(r), fake, fake,
+                              1 << 30, None) == -1
     W = L.Q4WeightsC()
-    W.E, W.d, W.f, W.f_s = 8, 200, 128, 0   # d not a multiple of 128
+    W.E, W.d, W.f, W.f_s = 8, 256, 128, 128  # shared expert declared but pointers NULL
     for m in (W.gate_up, W.down):
         m.qw = m.scale = m.bias = fake
-    assert lib.moe_expert_ffn(fake, 16, 200, ctypes.byref(W), ctypes.byref(r), fake, fake,
-                              1 << 30, None) == -2
-    W.d, W.f_s = 256, 128                    # shared expert declared but pointers NULL
-    assert lib.moe_expert_ffn(fake, 16, 256, ctypes.byref(W), ctypes.byref(r), fake, fake,
-                              1 << 30, None) == -1
+    assert lib.moe_q4_prepack(ctypes.byref(W), fake, 1 << 30, None) == -1
+    W.f_s = 0
+    assert lib.moe_q4_prepack(ctypes.byref(W), fake, 16, None) == -3   # destination too small
+    # the kernel-native copy has exactly the bytes of the interchange arrays
+    E, d, f, fs = 256, 2048, 512, 512
+    inter = (E * 2 * f * d // 2 + E * 2 * f * (d // 64) * 4 + E * d * f // 2 + E * d * (f // 64) * 4
+             + 2 * fs * d // 2 + 2 * fs * (d // 64) * 4 + d * fs // 2 + d * (fs // 64) * 4)
+    assert L.moe_q4_packed_size(E, d, f, fs) == inter

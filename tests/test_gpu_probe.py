@@ -86,3 +86,46 @@ def test_tmem_16x256b_fragment_layout():
                         col = 8 * j + 2 * (t % 4) + (r & 1)
                         want[32 * q + t, 16 * half + 4 * j + r] = (lane << 16) | col
     assert np.array_equal(got, want)
+
+
+def _pack_reference(qw, scale, bias, kind, F_or_d):
+    """The kernel-native layout, built from its description in include/moeq4.h."""
+    E, R, W8 = qw.shape
+    K = W8 * 8
+    nch, units = K // 64, R // 256
+    e, p, c, t, L = np.meshgrid(np.arange(E), np.arange(units), np.arange(nch), np.arange(2),
+                                np.arange(128), indexing="ij")
+    if kind == 0:
+        row = ((L >> 3) & 1) * F_or_d + 64 * (2 * p + t) + 8 * (L >> 4) + (L & 7)
+    else:
+        row = 256 * p + 128 * t + L
+    words = qw[e[..., None], row[..., None], c[..., None] * 8 + np.arange(8)]      # [..., 8]
+    nib = (words[..., None] >> (4 * np.arange(8, dtype=np.uint32))) & 15          # [..., 8 words, 8 nibbles]
+    order = np.array([0, 2, 4, 6, 1, 3, 5, 7])
+    perm = np.bitwise_or.reduce(nib[..., order] << (4 * np.arange(8, dtype=np.uint32)), axis=-1)
+    perm = perm.astype(np.uint32)
+    sw = ((L >> 2) & 1)[..., None]
+    halves = perm.reshape(*perm.shape[:-1], 2, 4)
+    stored = np.where(sw[..., None] == 1, halves[..., ::-1, :], halves)             # [..., 2, 4]
+    codes = stored.reshape(E, units, nch, 2, 128, 8).astype("<u4").view(np.uint8)
+    codes = codes.reshape(E, units, nch, 2 * 128 * 32)
+    g = row * nch + c
+    sb = scale.reshape(E, -1)[e, g].astype(np.uint32) | (bias.reshape(E, -1)[e, g].astype(np.uint32) << 16)
+    sb = sb.astype("<u4").reshape(E, units, nch, 256).view(np.uint8)
+    return np.concatenate([codes, sb], axis=-1).reshape(-1)
+
+
+def test_prepack_matches_documented_layout():
+    import dataclasses
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], f_s=256, f=256, d=512)
+    W = synth.gen_weights(cfg)
+    dw = moeq4.DeviceWeights.from_host(W)
+    torch.cuda.synchronize()
+    got = dw.packed.cpu().numpy()
+    ref = np.concatenate([
+        _pack_reference(W.gu_qw, W.gu_scale, W.gu_bias, 0, cfg.f),
+        _pack_reference(W.dn_qw, W.dn_scale, W.dn_bias, 1, cfg.d),
+        _pack_reference(W.sgu_qw, W.sgu_scale, W.sgu_bias, 0, cfg.f_s),
+        _pack_reference(W.sdn_qw, W.sdn_scale, W.sdn_bias, 1, cfg.d)])
+    assert got.shape == ref.shape
+    assert np.array_equal(got, ref)
