@@ -14,14 +14,19 @@
 //
 // Data movement (TMA instructions cost the issuing warp tens of cycles each, so
 // the bytes per instruction and the number of issuing warps set the rate):
-//   packed weights  one 9 KB bulk copy per K-chunk (kernel-native layout)
+//   packed weights  one 9 KB bulk copy per K-chunk (kernel-native layout) into a
+//                   12-deep ring released as soon as the dequant warps have read it
 //   token rows      gate/up pass: gather4 of x rows; down pass: 16-row tiles of
-//                   the tile-padded activation rows; issued by six warps
+//                   the tile-padded activation rows; issued by five warps
+// A chunk slot (4 of them) pairs the chunk's token rows in shared memory with its
+// A stage in tensor memory: one `ready` barrier collects the token-row bytes and
+// the eight dequant warps, one `consumed` commit frees both, so the single MMA
+// thread waits once and commits once per chunk.
 //
 // Warp roles (608 threads, one CTA per SM, persistent over units):
 //   warps 0-7    dequantisation: warp w fills A tile w/4, TMEM lane quarter w%4
 //   warps 8-11   epilogue, lane quarter w-8
-//   warps 12-17  producers
+//   warps 12-17  producers (12: packed weights, 13-17: token rows)
 //   warp 18      TMEM allocator and single-thread MMA issuer
 // Tensor memory: columns [0, 256) hold 4 A stages of 64 columns (two tiles of
 // 128 rows x 64 bf16), [256, 512) the two accumulators (A tile j -> 256 + 128 j).
@@ -52,8 +57,8 @@ namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kNMax = 128;                 // rows per unit (MMA N)
-constexpr int kStages = 6;                 // shared-memory ring depth
-constexpr int kAStages = 4;                // TMEM A stages
+constexpr int kWStages = 12;               // packed-weight ring depth (released by the dequant warps)
+constexpr int kAStages = 4;                // chunk slots: token rows in smem + A stage in TMEM
 constexpr int kACols = 64;                 // TMEM columns per A stage (two tiles x 32)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator of tile j at column 256 + 128 j
@@ -70,15 +75,15 @@ constexpr int kBBytes = kNMax * 128;       // token rows: 64 bf16 (128 B) each, 
 constexpr int kABytes = kPackChunkBytes;   // one packed K-chunk of the unit
 constexpr int kEpiBytes = 32768;           // pass 0: 2 act tiles [128][64] bf16; pass 1: 4 x [32][32] fp32
 constexpr size_t kOffB = 0;
-constexpr size_t kOffA = kOffB + size_t(kStages) * kBBytes;
-constexpr size_t kOffEpi = (kOffA + size_t(kStages) * kABytes + 1023) / 1024 * 1024;
+constexpr size_t kOffA = kOffB + size_t(kAStages) * kBBytes;
+constexpr size_t kOffEpi = (kOffA + size_t(kWStages) * kABytes + 1023) / 1024 * 1024;
 constexpr size_t kOffCtl = kOffEpi + kEpiBytes;
 
 struct Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t a_full[kAStages];
-  uint64_t a_empty[kAStages];
+  uint64_t full_w[kWStages];    // packed weights landed
+  uint64_t empty_w[kWStages];   // packed weights read by all dequant warps
+  uint64_t ready[kAStages];     // slot's token rows landed and its A stage written
+  uint64_t consumed[kAStages];  // slot's MMAs retired: token rows and A stage free
   uint64_t d_full;
   uint64_t d_empty[2];
   uint64_t epi_bar;
@@ -179,13 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], kDqWarps + 1);
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&ctl.full_w[s], 1);
+      mbar_init(&ctl.empty_w[s], kDqWarps);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&ctl.a_full[s], kDqWarps);
-      mbar_init(&ctl.a_empty[s], 1);
+      mbar_init(&ctl.ready[s], 1 + kDqWarps);   // token-row bytes + one arrival, 8 dequant warps
+      mbar_init(&ctl.consumed[s], 1);
     }
     mbar_init(&ctl.d_full, 1);
     mbar_init(&ctl.d_empty[0], kEpiWarps);
@@ -222,7 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
     // ------------------------------------------------------------- producers
+    // warp 0 of the group streams the packed weights; the others the token rows
     const int pw = warp - kProdWarp0;
+    const bool wprod = pw == 0;
+    const uint32_t nring = wprod ? kWStages : kAStages;
+    uint64_t* fullr = wprod ? ctl.full_w : ctl.ready;
+    uint64_t* emptyr = wprod ? ctl.empty_w : ctl.consumed;
     const uint64_t pol_x = policy_evict_last();   // token rows: reused by every unit of a tile
     uint32_t it = 0;
     bool ok = true;
@@ -237,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* mB = U.shared ? &tmB_sh : &tmB;
       // this lane's token-row copy for every chunk of the unit (at most one)
       const int nops = MODE == 0 ? npad / 4 : npad / 16;
-      const int g = kProdWarps * lane + pw;
-      const bool has_op = g < nops;
+      const int g = (kProdWarps - 1) * lane + (pw - 1);
+      const bool has_op = !wprod && g < nops;
       int r4[4] = {0, 0, 0, 0};
       if (has_op) {
         if (MODE == 0) {
@@ -251,42 +261,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           r4[0] = U.act0 + 16 * g;
         }
       }
-      const uint32_t bytes = kABytes + npad * 128;
       const int nch = U.K / 64;
       for (int c = 0; c < nch; ++c, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
-        if (!__all_sync(kFull, mbar_wait(&ctl.empty[s], ph ^ 1u, abortp, lim))) {
+        const int s = it % nring;
+        const uint32_t ph = (it / nring) & 1u;
+        if (!__all_sync(kFull, mbar_wait(&emptyr[s], ph ^ 1u, abortp, lim))) {
           if (lane == 0) raise_abort(ctl, a.err);
           ok = false;
           break;
         }
-        if (pw == 0 && lane == 0) {
-          mbar_arrive_expect_tx(&ctl.full[s], bytes);
-          bulk_load(sA + s * kABytes, blocks + static_cast<size_t>(c) * kABytes, kABytes,
-                    &ctl.full[s]);
-        }
-        if (has_op) {
-          uint8_t* dB = sB + s * kBBytes;
-          if (MODE == 0)
-            tma_gather4(dB + g * 512, mB, &ctl.full[s], c * 64, r4[0], r4[1], r4[2], r4[3], pol_x);
-          else
-            tma_load_2d(dB + g * 2048, mB, &ctl.full[s], c * 64, r4[0], pol_x);
+        if (wprod) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&fullr[s], kABytes);
+            bulk_load(sA + s * kABytes, blocks + static_cast<size_t>(c) * kABytes, kABytes,
+                      &fullr[s]);
+          }
+        } else {
+          if (pw == 1 && lane == 0) mbar_arrive_expect_tx(&fullr[s], npad * 128);
+          if (has_op) {
+            uint8_t* dB = sB + s * kBBytes;
+            if (MODE == 0)
+              tma_gather4(dB + g * 512, mB, &fullr[s], c * 64, r4[0], r4[1], r4[2], r4[3], pol_x);
+            else
+              tma_load_2d(dB + g * 2048, mB, &fullr[s], c * 64, r4[0], pol_x);
+          }
         }
       }
     }
-    if (!ok && pw == 0 && lane == 0) {
+    if (!ok && pw <= 1 && lane == 0) {
       // let copies already in flight land before the CTA's shared memory goes away
-      const uint32_t n = it < static_cast<uint32_t>(kStages) ? it : kStages;
+      const uint32_t n = it < nring ? it : nring;
       for (uint32_t i = 1; i <= n; ++i) {
         const uint32_t j = it - i;
-        mbar_wait(&ctl.full[j % kStages], (j / kStages) & 1u, &ctl.zero, 20000000ull);
+        mbar_wait(&fullr[j % nring], (j / nring) & 1u, &ctl.zero, 20000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, ita = 0, nu = 0;
+      uint32_t it = 0, nu = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         Unit U;
@@ -294,13 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t npad = (U.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(128, npad);
         const int nch = U.K / 64;
-        for (int c = 0; c < nch && ok; ++c, ++it, ++ita) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          const int sa = ita % kAStages;
-          const uint32_t pha = (ita / kAStages) & 1u;
-          if (!mbar_wait(&ctl.full[s], ph, abortp, lim) ||
-              !mbar_wait(&ctl.a_full[sa], pha, abortp, lim)) {
+        for (int c = 0; c < nch && ok; ++c, ++it) {
+          const int s = it % kAStages;
+          const uint32_t ph = (it / kAStages) & 1u;
+          if (!mbar_wait(&ctl.ready[s], ph, abortp, lim)) {
             raise_abort(ctl, a.err);
             ok = false;
             break;
@@ -318,14 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             const uint32_t dcol = tmem + kDCol + 128 * j;
-            const uint32_t acol = tmem + sa * kACols + 32 * j;
+            const uint32_t acol = tmem + s * kACols + 32 * j;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(dcol, acol + kk * 8, sdesc_k_sw128(bsm + kk * 32), idesc, (c | kk) != 0);
           }
           if (!ok) break;
-          mma_commit(&ctl.empty[s]);
-          mma_commit(&ctl.a_empty[sa]);
+          mma_commit(&ctl.consumed[s]);
         }
         if (!ok) break;
         mma_commit(&ctl.d_full);
@@ -343,54 +352,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = q * 32 + lane;      // TMEM lane = A row
     const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j;
     const int sw = (L >> 2) & 1;      // the row's 16-byte halves are stored swapped when set
-    uint32_t it = 0, ita = 0;
+    // Software pipeline over the CTA's whole chunk sequence: the packed words of
+    // chunk i+1 are fetched before chunk i is expanded, and the tensor-memory
+    // stores of chunk i are waited for only after chunk i+1's arithmetic.
+    uint32_t it_load = 0;          // next chunk whose packed words are fetched
+    uint32_t it_done = 0;          // chunks expanded so far
+    int pend_sa = -1;              // A stage whose stores are still in flight
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+    uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+    uint32_t sbw = 0;
+    // total chunks of this CTA
+    uint32_t n_chunks = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       Unit U;
-      if (!decode_unit(a, n_rt, u, U)) continue;
-      const int nch = U.K / 64;
-      for (int c = 0; c < nch; ++c, ++it, ++ita) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
-        const int sa = ita % kAStages;
-        const uint32_t pha = (ita / kAStages) & 1u;
-        if (!__all_sync(kFull, mbar_wait(&ctl.full[s], ph, abortp, lim))) {
-          if (lane == 0) raise_abort(ctl, a.err);
+      if (decode_unit(a, n_rt, u, U)) n_chunks += U.K / 64;
+    }
+    auto fetch = [&](uint32_t i) -> bool {   // packed words of chunk i into h0, h1, sbw
+      const int s = i % kWStages;
+      const uint32_t ph = (i / kWStages) & 1u;
+      if (!__all_sync(kFull, mbar_wait(&ctl.full_w[s], ph, abortp, lim))) return false;
+      const uint8_t* blk = sA + s * kABytes;
+      const uint8_t* rowp = blk + j * 4096 + L * 32;
+      h0 = *reinterpret_cast<const uint4*>(rowp + 16 * sw);
+      h1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 - sw));
+      sbw = reinterpret_cast<const uint32_t*>(blk + 8192)[j * 128 + L];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.empty_w[s]);
+      return true;
+    };
+    if (n_chunks > 0) ok = fetch(it_load++);
+    while (ok && it_done < n_chunks) {
+      const uint4 c0 = h0, c1 = h1;
+      const uint32_t csb = sbw;
+      if (it_load < n_chunks) {
+        if (!fetch(it_load++)) {
           ok = false;
           break;
         }
-        const uint8_t* blk = sA + s * kABytes;
-        const uint8_t* rowp = blk + j * 4096 + L * 32;
-        const uint4 h0 = *reinterpret_cast<const uint4*>(rowp + 16 * sw);
-        const uint4 h1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 - sw));
-        const uint32_t sbw = reinterpret_cast<const uint32_t*>(blk + 8192)[j * 128 + L];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.empty[s]);
-        if (!__all_sync(kFull, mbar_wait(&ctl.a_empty[sa], pha ^ 1u, abortp, lim))) {
-          if (lane == 0) raise_abort(ctl, a.err);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t s2 = bf16_pair(static_cast<uint16_t>(sbw & 0xFFFFu));
-        const uint32_t b2 = bf16_pair(static_cast<uint16_t>(sbw >> 16));
-        uint32_t v[16];
-        dequant8(h0.x, s2, b2, v + 0);
-        dequant8(h0.y, s2, b2, v + 4);
-        dequant8(h0.z, s2, b2, v + 8);
-        dequant8(h0.w, s2, b2, v + 12);
-        tmem_st_32x32b_x16(taddr + sa * kACols, v);
-        dequant8(h1.x, s2, b2, v + 0);
-        dequant8(h1.y, s2, b2, v + 4);
-        dequant8(h1.z, s2, b2, v + 8);
-        dequant8(h1.w, s2, b2, v + 12);
-        tmem_st_32x32b_x16(taddr + sa * kACols + 16, v);
+      }
+      const uint32_t s2 = bf16_pair(static_cast<uint16_t>(csb & 0xFFFFu));
+      const uint32_t b2 = bf16_pair(static_cast<uint16_t>(csb >> 16));
+      uint32_t v[32];
+      dequant8(c0.x, s2, b2, v + 0);
+      dequant8(c0.y, s2, b2, v + 4);
+      dequant8(c0.z, s2, b2, v + 8);
+      dequant8(c0.w, s2, b2, v + 12);
+      dequant8(c1.x, s2, b2, v + 16);
+      dequant8(c1.y, s2, b2, v + 20);
+      dequant8(c1.z, s2, b2, v + 24);
+      dequant8(c1.w, s2, b2, v + 28);
+      if (pend_sa >= 0) {            // publish the previous chunk's A stage
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.a_full[sa]);
+        if (lane == 0) mbar_arrive(&ctl.ready[pend_sa]);
       }
+      const int sa = it_done % kAStages;
+      const uint32_t pha = (it_done / kAStages) & 1u;
+      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[sa], pha ^ 1u, abortp, lim))) {
+        ok = false;
+        pend_sa = -1;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_32x32b_x16(taddr + sa * kACols, *reinterpret_cast<const uint32_t(*)[16]>(v));
+      tmem_st_32x32b_x16(taddr + sa * kACols + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
+      pend_sa = sa;
+      ++it_done;
     }
+    if (pend_sa >= 0) {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.ready[pend_sa]);
+    }
+    if (!ok && lane == 0) raise_abort(ctl, a.err);
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ------------------------------------------------------------- epilogue
     const int q = warp - kEpiWarp0;
