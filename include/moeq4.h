@@ -44,6 +44,7 @@ typedef int32_t moe_status;
 #define MOE_ERR_DEVICE       -5  /* device error word is non-zero (moe_get_device_error) */
 #define MOE_ERR_UNSUPPORTED  -6  /* current device is not sm_103 */
 #define MOE_ERR_ALIGN        -7  /* a pointer is not 16-byte aligned */
+#define MOE_ERR_TOO_LARGE    -8  /* sizes exceed the fixed scratch of moe_route_noalloc */
 
 /* Bits of the device error word. */
 #define MOE_DEVERR_NONFINITE_LOGIT  1  /* a router logit was NaN/Inf (treated as -inf) */
@@ -161,6 +162,23 @@ size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int3
  * and inv may then be NULL). */
 moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, size_t ws_bytes,
                      void* stream);
+
+/* moe_route for callers that cannot allocate device memory. The pages have no
+ * counterpart; this entry exists for code that may not call cudaMalloc at all,
+ * such as a serving process that reserves all device memory up front and hands
+ * out fixed arenas, or a plugin that has no access to its host framework's
+ * allocator. Same inputs, outputs and results as moe_route, but its scratch is
+ * a fixed array inside the library (about 770 KB, held on every GPU that loads
+ * the library until the process exits), so:
+ *  - sizes are limited to T <= 8192, E <= 256, k <= 8; larger ones return
+ *    MOE_ERR_TOO_LARGE and enqueue nothing;
+ *  - the first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture;
+ *  - every call shares the one array: each call first clears the part that
+ *    must start at zero, and calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race and must be serialised by the caller;
+ *  - it calls no cudaMalloc, cudaFree or allocating library routine. */
+moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void* stream);
 
 /* Grouped expert FFN with in-kernel 4-bit dequantisation ([A] §5-1: weights stay
  * packed, dequantised tile by tile on chip, FP32 accumulation; [C] "Qwen 구조와

@@ -275,6 +275,32 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// ---- fixed scratch for moe_route_noalloc (no counterpart on the pages)
+constexpr int kNoAllocMaxT = 8192;
+constexpr int kNoAllocMaxE = 256;
+constexpr int kNoAllocMaxK = 8;
+// routing scratch at the limits: lookback words and block bases of 256 blocks x 256
+// experts, 2 counters, local ranks of 65536 rows (each area 256-byte aligned)
+constexpr size_t kNoAllocBytes = 262144 + 256 + 262144 + 262144;
+__device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
+
+// Device address of g_route_scratch on the current device, looked up once per
+// device with that device current (host code cannot use the symbol itself).
+moe_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> g(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MOE_OK;
+}
+
 std::mutex g_ev_mu;
 cudaEvent_t g_events[8] = {};
 int g_nevents = 0;
@@ -398,6 +424,21 @@ moe_status moe_debug_set_stage_events(void* const* events, int32_t n) {
   return MOE_OK;
 }
 
+moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void* stream) {
+  moe_status st = check_route_out(out);
+  if (st != MOE_OK) return st;
+  if (out->T > kNoAllocMaxT || out->E > kNoAllocMaxE || out->k > kNoAllocMaxK)
+    return MOE_ERR_TOO_LARGE;
+  const RouteWs L = route_ws_layout(out->T, out->E, out->k);
+  if (L.total > kNoAllocBytes) return MOE_ERR_TOO_LARGE;
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the lookback words and counters must start at zero (each call also leaves them zero)
+  if (cudaMemsetAsync(ws, 0, L.blk_base, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return route_impl(logits, out, ws, kNoAllocBytes, s);
+}
+
 const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "ok";
@@ -408,6 +449,8 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_DEVICE: return "device error word is set";
     case MOE_ERR_UNSUPPORTED: return "device is not sm_103";
     case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_TOO_LARGE:
+      return "sizes exceed the fixed scratch of moe_route_noalloc (T <= 8192, E <= 256, k <= 8)";
     default: return "unknown status";
   }
 }

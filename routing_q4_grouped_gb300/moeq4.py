@@ -23,6 +23,7 @@ MOE_DEVERR_SCAN_TIMEOUT = 2
 MOE_DEVERR_PIPE_TIMEOUT = 4
 MOE_DEVERR_BAD_TILE = 8
 MOE_DEVERR_BAD_WORKSPACE = 16
+MOE_ERR_TOO_LARGE = -8
 
 _c_i32 = ctypes.c_int32
 _c_ptr = ctypes.c_void_p
@@ -63,6 +64,7 @@ _SIGS = {
     "moe_ffn_workspace_size": (_c_size, [_c_i32] * 7),
     "moe_layer_workspace_size": (_c_size, [_c_i32] * 7),
     "moe_route": (_c_i32, [_c_ptr, ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
+    "moe_route_noalloc": (_c_i32, [_c_ptr, ctypes.POINTER(RouteOutC), _c_ptr]),
     "moe_q4_packed_size": (_c_size, [_c_i32] * 4),
     "moe_q4_prepack": (_c_i32, [ctypes.POINTER(Q4WeightsC), _c_ptr, _c_size, _c_ptr]),
     "moe_expert_ffn": (_c_i32, [_c_ptr, _c_i32, _c_i32, ctypes.POINTER(Q4PackedC),
@@ -239,6 +241,17 @@ def moe_route(logits: torch.Tensor, out: RouteBuffers, ws: torch.Tensor, stream=
     c = out.cstruct()
     _check("moe_route", lib().moe_route(_ptr(logits), ctypes.byref(c), _ptr(ws), ws.numel(),
                                         _stream(stream)))
+
+
+def moe_route_noalloc(logits: torch.Tensor, out: RouteBuffers, stream=None) -> None:
+    """moe_route with the library's fixed internal scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; limited to T <= 8192,
+    E <= 256, k <= 8. Calls that overlap on the GPU share the scratch and race.
+    """
+    assert logits.dtype == torch.float32 and logits.is_contiguous()
+    c = out.cstruct()
+    _check("moe_route_noalloc", lib().moe_route_noalloc(_ptr(logits), ctypes.byref(c), _stream(stream)))
 
 
 def moe_expert_ffn(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.Tensor,
