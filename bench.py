@@ -184,7 +184,7 @@ def max_over_ranks(world, v):
 def oracle_sample(cfg, n_groups, first_group, block_m):
     """Times the oracle on a bounded sample of one layer and scales it to the
     whole layer by rows: routing of all T tokens, then the FFN of `n_groups`
-    consecutive routed expert groups. Returns (seconds for the full layer, note)."""
+    routed expert groups of about the mean size. Returns (seconds for the full layer, note)."""
     import oracle as O
     from routing_q4_grouped_gb300 import synth
 
@@ -195,8 +195,9 @@ def oracle_sample(cfg, n_groups, first_group, block_m):
     t0 = time.perf_counter()
     r = O.route(logits, cfg.k, block_m)
     t_route = time.perf_counter() - t0
-    groups = [(first_group + i) % cfg.E for i in range(n_groups)]
-    groups = [g for g in groups if r.counts[g] > 0] or [int(np.argmax(r.counts))]
+    # representative groups: the experts whose row counts are closest to the mean
+    near = np.argsort(np.abs(r.counts - r.counts.mean()), kind="stable")[: max(16, n_groups)]
+    groups = [int(near[(first_group + i) % len(near)]) for i in range(n_groups)]
     rows = int(sum(r.counts[g] for g in groups))
     t0 = time.perf_counter()
     O.expert_ffn(x, W, r, experts=groups, shared=False)
