@@ -301,22 +301,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, nu = 0;
       bool ok = true;
+      // B descriptors advance linearly: slot s adds kBBytes/16, K-step kk adds 32/16
+      const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
+      bool next_ready = false;   // ready[] of chunk `it` already observed
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         Unit U;
         if (!decode_unit(a, n_rt, u, U)) continue;
         const uint32_t npad = (U.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(128, npad);
         const int nch = U.K / 64;
-        for (int c = 0; c < nch && ok; ++c, ++it) {
+        for (int c = 0; c < nch; ++c, ++it) {
           const int s = it % kAStages;
           const uint32_t ph = (it / kAStages) & 1u;
-          if (!mbar_wait(&ctl.ready[s], ph, abortp, lim)) {
+          if (!next_ready && !mbar_wait(&ctl.ready[s], ph, abortp, lim)) {
             raise_abort(ctl, a.err);
             ok = false;
             break;
           }
+          // probe the next chunk's slot now; the answer is used after this chunk's MMAs
+          const uint32_t s1 = (it + 1) % kAStages;
+          next_ready = mbar_test(&ctl.ready[s1], ((it + 1) / kAStages) & 1u);
           tc_fence_after();
-          const uint32_t bsm = smem_u32(sB + s * kBBytes);
+          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s) * (kBBytes >> 4);
+          const uint32_t acc0 = c != 0;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (c == 0) {   // the epilogue must have drained this accumulator
@@ -329,9 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t dcol = tmem + kDCol + 128 * j;
             const uint32_t acol = tmem + s * kACols + 32 * j;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(dcol, acol + kk * 8, sdesc_k_sw128(bsm + kk * 32), idesc, (c | kk) != 0);
+            mma_ts(dcol, acol, bdesc, idesc, acc0);
+            mma_ts(dcol, acol + 8, bdesc + 2, idesc, 1);
+            mma_ts(dcol, acol + 16, bdesc + 4, idesc, 1);
+            mma_ts(dcol, acol + 24, bdesc + 6, idesc, 1);
           }
           if (!ok) break;
           mma_commit(&ctl.consumed[s]);

@@ -147,7 +147,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
     __syncthreads();
   }
 
-  // ---- decoupled lookback over blocks, one column per expert
+  // ---- decoupled lookback over blocks, one column per expert. Predecessor
+  // words are read kLookback at a time (independent loads), then consumed in
+  // order: aggregates are added, an inclusive prefix ends the walk, a word not
+  // yet published is re-read (bounded in time).
+  constexpr int kLookback = 16;
   for (int e = tid; e < E; e += kRouteThreads) {
     const uint32_t cnt = static_cast<uint32_t>(sCnt[e]);
     uint32_t* mine = a.lb + static_cast<size_t>(b) * E + e;
@@ -157,24 +161,34 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
     } else {
       st_release(mine, kLbAggregate | cnt);
       int p = b - 1;
-      uint32_t spins = 0;
       uint64_t t_start = 0;
-      while (p >= 0) {
-        const uint32_t word = ld_acquire(a.lb + static_cast<size_t>(p) * E + e);
-        const uint32_t st = word & ~kLbValueMask;
-        if (st == 0) {
-          if ((++spins & 255u) == 0) {
+      uint32_t spins = 0;
+      bool done = false;
+      while (!done && p >= 0) {
+        uint32_t word[kLookback];
+#pragma unroll
+        for (int i = 0; i < kLookback; ++i)
+          word[i] = (p - i >= 0) ? ld_acquire(a.lb + static_cast<size_t>(p - i) * E + e) : kLbInclusive;
+        int used = 0;
+#pragma unroll
+        for (int i = 0; i < kLookback; ++i) {
+          if (done || used < i) continue;          // stop at the first word not yet published
+          const uint32_t st = word[i] & ~kLbValueMask;
+          if (st == 0) continue;
+          excl += word[i] & kLbValueMask;
+          used = i + 1;
+          if (st == kLbInclusive) done = true;
+        }
+        p -= used;
+        if (!done && used < kLookback && p >= 0) {   // a predecessor has not published yet
+          if ((++spins & 15u) == 0) {
             if (t_start == 0) t_start = globaltimer_ns();
             else if (globaltimer_ns() - t_start > a.timeout_ns) {
               atomicOr(a.err, MOE_DEVERR_SCAN_TIMEOUT);
               break;
             }
           }
-          continue;
         }
-        excl += word & kLbValueMask;
-        if (st == kLbInclusive) break;
-        --p;
       }
       st_release(mine, kLbInclusive | (excl + cnt));
     }
