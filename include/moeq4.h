@@ -83,10 +83,9 @@ typedef struct moe_q4_weights {
  * produced once by moe_q4_prepack (values unchanged; only their order differs).
  * Each matrix [R][K] is cut into units of 256 rows (two 128-row tiles) and
  * K-chunks of 64; chunk c of unit u is one contiguous 9216-byte block:
- *   bytes [0, 8192)     codes of tile 0 then tile 1: 128 rows x 32 bytes, the
- *                       row's two 16-byte halves swapped when bit 2 of the row
- *                       index is set, nibbles of each word in the order
- *                       k0 k2 k4 k6 k1 k3 k5 k7
+ *   bytes [0, 8192)     codes of tile 0 then tile 1; per tile, K 0-31 of its
+ *                       128 rows (16 bytes each, row-major) then K 32-63;
+ *                       nibbles of each word in the order k0 k2 k4 k6 k1 k3 k5 k7
  *   bytes [8192, 9216)  2 x 128 words: scale | bias << 16 (bf16 bits)
  * Row i of tile t of unit p of expert e is, for gate/up (F = f or f_s),
  *   e*2F + up*F + 64*(2p + t) + 8*(i >> 4) + (i & 7), up = (i >> 3) & 1

@@ -12,26 +12,29 @@
 // into tensor memory (tcgen05.st) as the MMA's A operand: no bf16 weight tile
 // touches shared or global memory.
 //
-// Data movement (TMA instructions cost the issuing warp tens of cycles each, so
-// the bytes per instruction and the number of issuing warps set the rate):
-//   packed weights  one 9 KB bulk copy per K-chunk (kernel-native layout) into a
-//                   12-deep ring released as soon as the dequant warps have read it
+// The pipeline advances in pairs of K-chunks (K = 128), so every barrier wait is
+// paid once per two quantisation groups:
+//   packed weights  read by the dequant warps themselves, one pair ahead, with
+//                   16-byte loads (each warp load covers 512 contiguous bytes);
+//                   an L2 bulk prefetch of the next unit's blocks hides HBM latency
 //   token rows      gate/up pass: gather4 of x rows; down pass: 16-row tiles of
-//                   the tile-padded activation rows; issued by five warps
-// A chunk slot (4 of them) pairs the chunk's token rows in shared memory with its
-// A stage in tensor memory: one `ready` barrier collects the token-row bytes and
-// the eight dequant warps, one `consumed` commit frees both, so the single MMA
-// thread waits once and commits once per chunk.
+//                   the tile-padded activation rows; issued by seven warps
+// A pair slot (2 of them) joins the pair's token rows in shared memory with its
+// A stage in tensor memory: a `ready` barrier collects the sixteen dequant warps,
+// a `consumed` commit frees the stage; token rows have a deeper ring of their own.
 //
-// Warp roles (608 threads, one CTA per SM, persistent over units):
-//   warps 0-7    dequantisation: warp w fills A tile w/4, TMEM lane quarter w%4
-//   warps 8-11   epilogue, lane quarter w-8
-//   warps 12-17  producers (12: packed weights, 13-17: token rows)
-//   warp 18      TMEM allocator and single-thread MMA issuer
-// Tensor memory: columns [0, 256) hold 4 A stages of 64 columns (two tiles of
-// 128 rows x 64 bf16), [256, 512) the two accumulators (A tile j -> 256 + 128 j).
-// An accumulator is released as soon as the epilogue has read it, so the next
-// unit's MMAs on tile 0 overlap the epilogue of tile 1.
+// Warp roles (896 threads, one CTA per SM, persistent over units):
+//   warps 0-15   dequantisation: warp w expands chunk w/8 of every pair for A
+//                tile (w/4)%2, TMEM lane quarter w%4
+//   warps 16-19  epilogue, lane quarter w-16
+//   warps 20-26  producers of token rows (warp 20 also prefetches weights into L2)
+//   warp 27      TMEM allocator and MMA issuer: the whole warp runs the loop with
+//                warp-uniform operands and one elected lane issues each MMA, which
+//                keeps the tensor pipe fed back to back
+// Tensor memory: columns [0, 256) hold 2 pair stages of 128 columns (tile j,
+// chunk h of the pair at 64 j + 32 h), [256, 512) the two accumulators (A tile
+// j -> 256 + 128 j). An accumulator is released as soon as the epilogue has read
+// it, so the next unit's MMAs on tile 0 overlap the epilogue of tile 1.
 //
 // Pass 0 (gate/up): A tile j covers 64 output features with gate and up rows
 //   interleaved in blocks of 8 (TMEM lanes 16m..16m+7 = gate rows of features
@@ -57,34 +60,36 @@ namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kNMax = 128;                 // rows per unit (MMA N)
-constexpr int kWStages = 12;               // packed-weight ring depth (released by the dequant warps)
-constexpr int kAStages = 4;                // chunk slots: token rows in smem + A stage in TMEM
-constexpr int kACols = 64;                 // TMEM columns per A stage (two tiles x 32)
+constexpr int kStages = 4;                 // chunk stages of dequantised weights in TMEM
+constexpr int kBSlots = 4;                 // pair slots of token rows in shared memory
+constexpr int kACols = 64;                 // TMEM columns per chunk stage (2 tiles x 32)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator of tile j at column 256 + 128 j
-constexpr int kDqWarps = 8;
-constexpr int kEpiWarp0 = 8;
+constexpr int kDqWarps = 16;               // warp w: chunk w/8 of each pair, A tile (w/4)%2
+constexpr int kDqGroupWarps = 8;           // warps per chunk parity
+constexpr int kEpiWarp0 = 16;              // warp % 4 = TMEM lane quarter
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarp0 = 12;
+constexpr int kProdWarp0 = 20;
 constexpr int kProdWarps = 6;
-constexpr int kMmaWarp = 18;
-constexpr int kThreads = 19 * 32;
+constexpr int kMmaWarp0 = 26;              // two MMA issuers: warp 26 + chunk parity
+constexpr int kThreads = 28 * 32;
+constexpr uint32_t kHandoffBar0 = 1;       // named barriers 1, 2: MMA issue order handoff
 static_assert(kThreads == kGemmThreads, "thread count");
 
-constexpr int kBBytes = kNMax * 128;       // token rows: 64 bf16 (128 B) each, 128B swizzle
-constexpr int kABytes = kPackChunkBytes;   // one packed K-chunk of the unit
+constexpr int kBBytes = kNMax * 128;       // token rows of one K-chunk: 64 bf16 (128 B) each, 128B swizzle
+constexpr int kSlotBytes = 2 * kBBytes;    // a pair of K-chunks
 constexpr int kEpiBytes = 32768;           // pass 0: 2 act tiles [128][64] bf16; pass 1: 4 x [32][32] fp32
 constexpr size_t kOffB = 0;
-constexpr size_t kOffA = kOffB + size_t(kAStages) * kBBytes;
-constexpr size_t kOffEpi = (kOffA + size_t(kWStages) * kABytes + 1023) / 1024 * 1024;
+constexpr size_t kOffEpi = kOffB + size_t(kBSlots) * kSlotBytes;
 constexpr size_t kOffCtl = kOffEpi + kEpiBytes;
 
 struct Ctl {
-  uint64_t full_w[kWStages];    // packed weights landed
-  uint64_t empty_w[kWStages];   // packed weights read by all dequant warps
-  uint64_t ready[kAStages];     // slot's token rows landed and its A stage written
-  uint64_t consumed[kAStages];  // slot's MMAs retired: token rows and A stage free
-  uint64_t d_full;
+  uint64_t b_full[kBSlots];   // token-row slot landed (transaction bytes)
+  uint64_t b_empty[kBSlots];  // token-row slot's MMAs retired (both MMA warps)
+  uint64_t ready[kStages];    // chunk stage written by its dequant group
+  uint64_t consumed[kStages]; // chunk stage's MMAs retired
+  uint64_t d_full;            // both MMA warps committed the unit
+  uint64_t drain2;
   uint64_t d_empty[2];
   uint64_t epi_bar;
   uint64_t drain;
@@ -159,13 +164,57 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
+// Next (unit, pair) of this CTA's sequence; u starts at blockIdx.x - gridDim.x
+// with pi == npair == 0. Returns false when the sequence is exhausted.
+__device__ __forceinline__ bool next_pair(const GemmArgs& a, int n_rt, int total, int& u, int& pi,
+                                          int& npair, const uint8_t*& blocks) {
+  if (++pi < npair) return true;
+  for (u += gridDim.x; u < total; u += gridDim.x) {
+    Unit U;
+    if (decode_unit(a, n_rt, u, U)) {
+      pi = 0;
+      npair = U.K / 128;
+      blocks = unit_blocks(a, U);
+      return true;
+    }
+  }
+  return false;
+}
+
+// L2 prefetch of a unit's packed blocks, four K-chunks per request.
+__device__ __forceinline__ void prefetch_unit(const GemmArgs& a, const Unit& U) {
+  const uint8_t* b = unit_blocks(a, U);
+  const int nch = U.K / 64;
+  for (int c = 0; c < nch; c += 4)
+    bulk_prefetch_l2(b + static_cast<size_t>(c) * kPackChunkBytes,
+                     static_cast<uint32_t>(min(4, nch - c) * kPackChunkBytes));
+}
+
+// Packed words of one K-chunk for one lane: codes of K 0-31 and 32-63, scale|bias.
+struct ChunkWords {
+  uint4 lo, hi;
+  uint32_t sb;
+};
+
+__device__ __forceinline__ void load_chunk(const uint8_t* blk, uint32_t roff, uint32_t soff,
+                                           ChunkWords& w) {
+  w.lo = ld_nc_v4(blk + roff);
+  w.hi = ld_nc_v4(blk + roff + 2048);
+  w.sb = ld_nc_u32(blk + soff);
+}
+
+// 64 codes -> 32 bf16x2 words in K order.
+__device__ __forceinline__ void dequant_chunk(const ChunkWords& w, uint32_t (&v)[32]) {
+  const uint32_t s2 = bf16_pair(static_cast<uint16_t>(w.sb & 0xFFFFu));
+  const uint32_t b2 = bf16_pair(static_cast<uint16_t>(w.sb >> 16));
+  dequant8(w.lo.x, s2, b2, v + 0);
+  dequant8(w.lo.y, s2, b2, v + 4);
+  dequant8(w.lo.z, s2, b2, v + 8);
+  dequant8(w.lo.w, s2, b2, v + 12);
+  dequant8(w.hi.x, s2, b2, v + 16);
+  dequant8(w.hi.y, s2, b2, v + 20);
+  dequant8(w.hi.z, s2, b2, v + 24);
+  dequant8(w.hi.w, s2, b2, v + 28);
 }
 
 template <int MODE>
@@ -178,21 +227,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sB = smem + kOffB;
-  uint8_t* sA = smem + kOffA;
   uint8_t* sEpi = smem + kOffEpi;
   Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kWStages; ++s) {
-      mbar_init(&ctl.full_w[s], 1);
-      mbar_init(&ctl.empty_w[s], kDqWarps);
+    for (int s = 0; s < kBSlots; ++s) {
+      mbar_init(&ctl.b_full[s], 1);
+      mbar_init(&ctl.b_empty[s], 2);
     }
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&ctl.ready[s], 1 + kDqWarps);   // token-row bytes + one arrival, 8 dequant warps
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl.ready[s], kDqGroupWarps);
       mbar_init(&ctl.consumed[s], 1);
     }
-    mbar_init(&ctl.d_full, 1);
+    mbar_init(&ctl.d_full, 2);
+    mbar_init(&ctl.drain2, 1);
     mbar_init(&ctl.d_empty[0], kEpiWarps);
     mbar_init(&ctl.d_empty[1], kEpiWarps);
     mbar_init(&ctl.epi_bar, kEpiWarps);
@@ -201,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl.zero = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(&ctl.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -226,29 +275,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = n_rt * a.n_fb + a.n_sh_tiles * a.n_fb_sh;
 
   if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
-    // ------------------------------------------------------------- producers
-    // warp 0 of the group streams the packed weights; the others the token rows
+    // ---------------------------------------------------- token-row producers
     const int pw = warp - kProdWarp0;
-    const bool wprod = pw == 0;
-    const uint32_t nring = wprod ? kWStages : kAStages;
-    uint64_t* fullr = wprod ? ctl.full_w : ctl.ready;
-    uint64_t* emptyr = wprod ? ctl.empty_w : ctl.consumed;
+    const bool lead = pw == 0 && lane == 0;   // expect_tx, L2 prefetch, error reports
     const uint64_t pol_x = policy_evict_last();   // token rows: reused by every unit of a tile
-    uint32_t it = 0;
+    if (lead && static_cast<int>(blockIdx.x) < total) {
+      Unit U0;
+      if (decode_unit(a, n_rt, blockIdx.x, U0)) prefetch_unit(a, U0);
+    }
+    uint32_t ip = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
       if (!decode_unit(a, n_rt, u, U)) {
-        if (pw == 0 && lane == 0) atomicOr(a.err, MOE_DEVERR_BAD_TILE);
+        if (lead) atomicOr(a.err, MOE_DEVERR_BAD_TILE);
         continue;
       }
+      if (lead) {   // the next unit's weights head for L2 while this one runs
+        const int v = u + gridDim.x;
+        Unit V;
+        if (v < total && decode_unit(a, n_rt, v, V)) prefetch_unit(a, V);
+      }
       const int npad = (U.rows + 15) & ~15;
-      const uint8_t* blocks = unit_blocks(a, U);
       const CUtensorMap* mB = U.shared ? &tmB_sh : &tmB;
-      // this lane's token-row copy for every chunk of the unit (at most one)
+      // this lane's token-row copy for each chunk of the unit (at most one)
       const int nops = MODE == 0 ? npad / 4 : npad / 16;
-      const int g = (kProdWarps - 1) * lane + (pw - 1);
-      const bool has_op = !wprod && g < nops;
+      const int g = kProdWarps * lane + pw;
+      const bool has_op = g < nops;
       int r4[4] = {0, 0, 0, 0};
       if (has_op) {
         if (MODE == 0) {
@@ -261,178 +314,146 @@ __global__ void __launch_bounds__(kThreads, 1)
           r4[0] = U.act0 + 16 * g;
         }
       }
-      const int nch = U.K / 64;
-      for (int c = 0; c < nch; ++c, ++it) {
-        const int s = it % nring;
-        const uint32_t ph = (it / nring) & 1u;
-        if (!__all_sync(kFull, mbar_wait(&emptyr[s], ph ^ 1u, abortp, lim))) {
+      const int npair = U.K / 128;
+      for (int pi = 0; pi < npair; ++pi, ++ip) {
+        const uint32_t bs = ip % kBSlots;
+        if (!__all_sync(kFull,
+                        mbar_wait(&ctl.b_empty[bs], ((ip / kBSlots) & 1u) ^ 1u, abortp, lim))) {
           if (lane == 0) raise_abort(ctl, a.err);
           ok = false;
           break;
         }
-        if (wprod) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&fullr[s], kABytes);
-            bulk_load(sA + s * kABytes, blocks + static_cast<size_t>(c) * kABytes, kABytes,
-                      &fullr[s]);
-          }
-        } else {
-          if (pw == 1 && lane == 0) mbar_arrive_expect_tx(&fullr[s], npad * 128);
-          if (has_op) {
-            uint8_t* dB = sB + s * kBBytes;
-            if (MODE == 0)
-              tma_gather4(dB + g * 512, mB, &fullr[s], c * 64, r4[0], r4[1], r4[2], r4[3], pol_x);
-            else
-              tma_load_2d(dB + g * 2048, mB, &fullr[s], c * 64, r4[0], pol_x);
-          }
-        }
-      }
-    }
-    if (!ok && pw <= 1 && lane == 0) {
-      // let copies already in flight land before the CTA's shared memory goes away
-      const uint32_t n = it < nring ? it : nring;
-      for (uint32_t i = 1; i <= n; ++i) {
-        const uint32_t j = it - i;
-        mbar_wait(&fullr[j % nring], (j / nring) & 1u, &ctl.zero, 20000000ull);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, nu = 0;
-      bool ok = true;
-      // B descriptors advance linearly: slot s adds kBBytes/16, K-step kk adds 32/16
-      const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
-      bool next_ready = false;   // ready[] of chunk `it` already observed
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        Unit U;
-        if (!decode_unit(a, n_rt, u, U)) continue;
-        const uint32_t npad = (U.rows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(128, npad);
-        const int nch = U.K / 64;
-        for (int c = 0; c < nch; ++c, ++it) {
-          const int s = it % kAStages;
-          const uint32_t ph = (it / kAStages) & 1u;
-          if (!next_ready && !mbar_wait(&ctl.ready[s], ph, abortp, lim)) {
-            raise_abort(ctl, a.err);
-            ok = false;
-            break;
-          }
-          // probe the next chunk's slot now; the answer is used after this chunk's MMAs
-          const uint32_t s1 = (it + 1) % kAStages;
-          next_ready = mbar_test(&ctl.ready[s1], ((it + 1) / kAStages) & 1u);
-          tc_fence_after();
-          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s) * (kBBytes >> 4);
-          const uint32_t acc0 = c != 0;
+        if (lead) mbar_arrive_expect_tx(&ctl.b_full[bs], 2 * npad * 128);
+        if (has_op) {
+          uint8_t* dB = sB + bs * kSlotBytes;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (c == 0) {   // the epilogue must have drained this accumulator
-              if (!mbar_wait(&ctl.d_empty[j], (nu & 1u) ^ 1u, abortp, lim)) {
-                raise_abort(ctl, a.err);
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-            }
-            const uint32_t dcol = tmem + kDCol + 128 * j;
-            const uint32_t acol = tmem + s * kACols + 32 * j;
-            mma_ts(dcol, acol, bdesc, idesc, acc0);
-            mma_ts(dcol, acol + 8, bdesc + 2, idesc, 1);
-            mma_ts(dcol, acol + 16, bdesc + 4, idesc, 1);
-            mma_ts(dcol, acol + 24, bdesc + 6, idesc, 1);
+          for (int h = 0; h < 2; ++h) {
+            const int k0 = (2 * pi + h) * 64;
+            if (MODE == 0)
+              tma_gather4(dB + h * kBBytes + g * 512, mB, &ctl.b_full[bs], k0, r4[0], r4[1], r4[2],
+                          r4[3], pol_x);
+            else
+              tma_load_2d(dB + h * kBBytes + g * 2048, mB, &ctl.b_full[bs], k0, r4[0], pol_x);
           }
-          if (!ok) break;
-          mma_commit(&ctl.consumed[s]);
         }
-        if (!ok) break;
-        mma_commit(&ctl.d_full);
-        ++nu;
       }
-      // every issued MMA must retire before tensor memory is released
-      mma_commit(&ctl.drain);
-      mbar_wait(&ctl.drain, 0, &ctl.zero, lim);
     }
-    __syncwarp();
-  } else if (warp < kDqWarps) {
-    // ------------------------------------------------------ dequantisation
-    const int q = warp & 3;           // TMEM lane quarter
-    const int j = warp >> 2;          // A tile filled by this warp
-    const int L = q * 32 + lane;      // TMEM lane = A row
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j;
-    const int sw = (L >> 2) & 1;      // the row's 16-byte halves are stored swapped when set
-    // Software pipeline over the CTA's whole chunk sequence: the packed words of
-    // chunk i+1 are fetched before chunk i is expanded, and the tensor-memory
-    // stores of chunk i are waited for only after chunk i+1's arithmetic.
-    uint32_t it_load = 0;          // next chunk whose packed words are fetched
-    uint32_t it_done = 0;          // chunks expanded so far
-    int pend_sa = -1;              // A stage whose stores are still in flight
-    bool ok = true;
-    uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
-    uint32_t sbw = 0;
-    // total chunks of this CTA
+    if (!ok && lead) {
+      // let copies already in flight land before the CTA's shared memory goes away
+      const uint32_t n = ip < kBSlots ? ip : kBSlots;
+      for (uint32_t i = 1; i <= n; ++i) {
+        const uint32_t jp = ip - i;
+        mbar_wait(&ctl.b_full[jp % kBSlots], (jp / kBSlots) & 1u, &ctl.zero, 20000000ull);
+      }
+    }
+  } else if (warp >= kMmaWarp0) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp kMmaWarp0 + m issues chunk m of every pair, so chunks alternate
+    // between the two warps in K order: before chunk c it waits on named
+    // barrier kHandoffBar0 + m, which the other warp arrives at once it has
+    // issued chunk c-1. One warp's barrier waits thus overlap the other's MMAs.
+    // Each warp runs the loop with warp-uniform operands and one elected lane
+    // issues. Both warps walk the same pair sequence to its end, also after an
+    // abort, so every handoff is matched.
+    const uint32_t me = static_cast<uint32_t>(warp - kMmaWarp0);
     uint32_t n_chunks = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       Unit U;
       if (decode_unit(a, n_rt, u, U)) n_chunks += U.K / 64;
     }
-    auto fetch = [&](uint32_t i) -> bool {   // packed words of chunk i into h0, h1, sbw
-      const int s = i % kWStages;
-      const uint32_t ph = (i / kWStages) & 1u;
-      if (!__all_sync(kFull, mbar_wait(&ctl.full_w[s], ph, abortp, lim))) return false;
-      const uint8_t* blk = sA + s * kABytes;
-      const uint8_t* rowp = blk + j * 4096 + L * 32;
-      h0 = *reinterpret_cast<const uint4*>(rowp + 16 * sw);
-      h1 = *reinterpret_cast<const uint4*>(rowp + 16 * (1 - sw));
-      sbw = reinterpret_cast<const uint32_t*>(blk + 8192)[j * 128 + L];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.empty_w[s]);
-      return true;
-    };
-    if (n_chunks > 0) ok = fetch(it_load++);
-    while (ok && it_done < n_chunks) {
-      const uint4 c0 = h0, c1 = h1;
-      const uint32_t csb = sbw;
-      if (it_load < n_chunks) {
-        if (!fetch(it_load++)) {
+    uint32_t ip = 0, nu = 0;
+    bool ok = true;
+    const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB)) + me * (kBBytes >> 4);
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      Unit U;
+      if (!decode_unit(a, n_rt, u, U)) continue;
+      const uint32_t npad = (U.rows + 15) & ~15;
+      const uint32_t idesc = idesc_bf16_f32(128, npad);
+      const int npair = U.K / 128;
+      for (int pi = 0; pi < npair; ++pi, ++ip) {
+        const uint32_t c = 2 * ip + me;                 // chunk index in the CTA's sequence
+        const uint32_t bs = ip % kBSlots;
+        const uint32_t st = c % kStages;
+        // ready[st] also covers the pair's token rows (see the dequant warps)
+        if (ok) ok = __all_sync(kFull, mbar_wait(&ctl.ready[st], (c / kStages) & 1u, abortp, lim));
+        if (ok && pi == 0 && me == 0) {   // the epilogue must have drained both accumulators
+          ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[0], (nu & 1u) ^ 1u, abortp, lim)) &&
+               __all_sync(kFull, mbar_wait(&ctl.d_empty[1], (nu & 1u) ^ 1u, abortp, lim));
+        }
+        if (c > 0) named_bar_sync(kHandoffBar0 + me, 64);   // chunk c-1 has been issued
+        if (ok) {
+          tc_fence_after();
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>(bs) * (kSlotBytes >> 4);
+          mma_ts_chunk_elect(tmem + kDCol, tmem + kDCol + 128, tmem + st * kACols, bd, idesc,
+                             (pi | me) != 0);
+          mma_commit_elect(&ctl.consumed[st]);
+          mma_commit_elect(&ctl.b_empty[bs]);
+        } else if (lane == 0) {
+          raise_abort(ctl, a.err);
+        }
+        if (c + 1 < n_chunks) named_bar_arrive(kHandoffBar0 + (me ^ 1u), 64);
+      }
+      // each warp's commit covers its own MMAs; both together the whole unit
+      if (ok) mma_commit_elect(&ctl.d_full);
+      ++nu;
+    }
+    // every issued MMA must retire before tensor memory is released
+    uint64_t* dr = me ? &ctl.drain2 : &ctl.drain;
+    mma_commit_elect(dr);
+    mbar_wait(dr, 0, &ctl.zero, lim);
+    __syncwarp();
+  } else if (warp < kDqWarps) {
+    // ------------------------------------------------------ dequantisation
+    // Warp w expands chunk w/8 of every pair for A tile (w/4)%2, TMEM lane
+    // quarter w%4, so the two chunk parities form two groups that run half a
+    // pair apart. The ready barrier of a chunk completes once the group has
+    // stored it and (checked by the group's first warp) its token rows landed. The next pair's chunk is expanded into registers as soon as
+    // the current one is published: once a stage frees, only the tensor-memory
+    // stores stand between the MMAs and the next stage.
+    const int q = warp & 3;           // TMEM lane quarter
+    const int j = (warp >> 2) & 1;    // A tile
+    const int h = warp >> 3;          // chunk within the pair
+    const int L = q * 32 + lane;      // TMEM lane = A row
+    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j;
+    const uint32_t roff = h * kPackChunkBytes + j * 4096 + L * 16;          // row codes
+    const uint32_t soff = h * kPackChunkBytes + 8192 + (j * 128 + L) * 4;   // scale|bias
+    int cu = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), cpi = 0, cnp = 0;
+    const uint8_t* cbl = nullptr;
+    bool have = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+    ChunkWords n;                     // packed words of this warp's chunk of the next pair
+    if (have) load_chunk(cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes), roff, soff, n);
+    uint32_t ip = 0;
+    bool ok = true;
+    while (have) {
+      uint32_t v[32];
+      dequant_chunk(n, v);
+      const bool more = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+      if (more) load_chunk(cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes), roff, soff, n);
+      const uint32_t c = 2 * ip + h;                     // chunk index in the CTA's sequence
+      const uint32_t st = c % kStages;
+      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[st], ((c / kStages) & 1u) ^ 1u, abortp, lim))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t = tq + st * kACols;
+      tmem_st_32x32b_x16(t, *reinterpret_cast<const uint32_t(*)[16]>(v));
+      tmem_st_32x32b_x16(t + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
+      tmem_st_wait();
+      tc_fence_before();
+      if ((warp & 7) == 0) {
+        // the first warp of the group also vouches for the pair's token rows, so
+        // the MMA warps wait on a single barrier per chunk
+        const uint32_t bs = ip % kBSlots;
+        if (!__all_sync(kFull, mbar_wait(&ctl.b_full[bs], (ip / kBSlots) & 1u, abortp, lim))) {
           ok = false;
           break;
         }
       }
-      const uint32_t s2 = bf16_pair(static_cast<uint16_t>(csb & 0xFFFFu));
-      const uint32_t b2 = bf16_pair(static_cast<uint16_t>(csb >> 16));
-      uint32_t v[32];
-      dequant8(c0.x, s2, b2, v + 0);
-      dequant8(c0.y, s2, b2, v + 4);
-      dequant8(c0.z, s2, b2, v + 8);
-      dequant8(c0.w, s2, b2, v + 12);
-      dequant8(c1.x, s2, b2, v + 16);
-      dequant8(c1.y, s2, b2, v + 20);
-      dequant8(c1.z, s2, b2, v + 24);
-      dequant8(c1.w, s2, b2, v + 28);
-      if (pend_sa >= 0) {            // publish the previous chunk's A stage
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.ready[pend_sa]);
-      }
-      const int sa = it_done % kAStages;
-      const uint32_t pha = (it_done / kAStages) & 1u;
-      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[sa], pha ^ 1u, abortp, lim))) {
-        ok = false;
-        pend_sa = -1;
-        break;
-      }
-      tc_fence_after();
-      tmem_st_32x32b_x16(taddr + sa * kACols, *reinterpret_cast<const uint32_t(*)[16]>(v));
-      tmem_st_32x32b_x16(taddr + sa * kACols + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
-      pend_sa = sa;
-      ++it_done;
-    }
-    if (pend_sa >= 0) {
-      tmem_st_wait();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.ready[pend_sa]);
+      if (lane == 0) mbar_arrive(&ctl.ready[st]);
+      ++ip;
+      have = more;
     }
     if (!ok && lane == 0) raise_abort(ctl, a.err);
   } else if (warp < kEpiWarp0 + kEpiWarps) {
@@ -566,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -56,10 +56,11 @@ void stage_mark(int i, cudaStream_t s);
 // A matrix [R][K] (R weight rows, K reduction) is cut into units of 256 rows,
 // two 128-row A tiles whose row order is the TMEM lane order the GEMM uses, and
 // K-chunks of 64 (one quantisation group). Chunk c of unit u is one contiguous
-// block of kPackChunkBytes: the codes of tile 0 then tile 1 (128 rows x 32 B each;
-// the two 16-byte halves of row L swapped when bit 2 of L is set; nibbles of each
-// word in the order k0 k2 k4 k6 k1 k3 k5 k7), then 2 x 128 words (scale | bias << 16).
-// Blocks are ordered unit-major, chunk-minor.
+// block of kPackChunkBytes: the codes of tile 0 then tile 1, each as two 2 KB
+// halves (K 0-31, then K 32-63) of 128 rows x 16 B, so that the 32 lanes of a
+// warp reading rows 32q..32q+31 touch 512 contiguous bytes per load (nibbles of
+// each word in the order k0 k2 k4 k6 k1 k3 k5 k7); then 2 x 128 words
+// (scale | bias << 16). Blocks are ordered unit-major, chunk-minor.
 constexpr int kPackChunkBytes = 2 * 128 * 32 + 2 * 128 * 4;   // 9216
 
 struct PackedMat {
@@ -93,7 +94,7 @@ cudaError_t launch_prepack(const uint32_t* qw, const uint16_t* scale, const uint
 
 // ------------------------------------------------------------ grouped GEMM
 
-constexpr int kGemmThreads = 608;          // 8 dequant, 4 epilogue, 6 producer, 1 MMA warps
+constexpr int kGemmThreads = 896;          // 16 dequant, 4 epilogue, 7 producer, 1 MMA warps
 
 struct GemmArgs {
   int K;                    // reduction length of routed units (d: gate/up, f: down)

@@ -12,7 +12,7 @@
 namespace moeq4 {
 namespace {
 
-// One thread per (expert, unit, chunk, tile, lane): 32 bytes of codes + one scale|bias word.
+// One thread per (expert, unit, chunk, tile, lane): two 16-byte code halves + one scale|bias word.
 __global__ void __launch_bounds__(256) prepack_kernel(const uint32_t* __restrict__ qw,
                                                       const uint16_t* __restrict__ scale,
                                                       const uint16_t* __restrict__ bias,
@@ -33,15 +33,14 @@ __global__ void __launch_bounds__(256) prepack_kernel(const uint32_t* __restrict
     const int row = kind == 0 ? pack_row_gate_up(e, F_or_d, p, j, L) : pack_row_down(e, F_or_d, p, j, L);
     const uint32_t* src = qw + static_cast<size_t>(row) * (K / 8) + c * 8;
     uint8_t* blk = dst + (static_cast<size_t>(e * units + p) * nch + c) * kPackChunkBytes;
-    const int sw = (L >> 2) & 1;
     uint4 h0, h1;
     h0.x = permute_nibbles(src[0]); h0.y = permute_nibbles(src[1]);
     h0.z = permute_nibbles(src[2]); h0.w = permute_nibbles(src[3]);
     h1.x = permute_nibbles(src[4]); h1.y = permute_nibbles(src[5]);
     h1.z = permute_nibbles(src[6]); h1.w = permute_nibbles(src[7]);
-    uint8_t* rowp = blk + j * 4096 + L * 32;
-    *reinterpret_cast<uint4*>(rowp + 16 * sw) = h0;
-    *reinterpret_cast<uint4*>(rowp + 16 * (1 - sw)) = h1;
+    uint8_t* rowp = blk + j * 4096 + L * 16;
+    *reinterpret_cast<uint4*>(rowp) = h0;          // K 0-31 of the chunk
+    *reinterpret_cast<uint4*>(rowp + 2048) = h1;   // K 32-63
     const size_t g = static_cast<size_t>(row) * nch + c;
     reinterpret_cast<uint32_t*>(blk + 8192)[j * 128 + L] =
         static_cast<uint32_t>(scale[g]) | (static_cast<uint32_t>(bias[g]) << 16);

@@ -26,6 +26,9 @@ __device__ __forceinline__ uint32_t lane_id() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // ----------------------------------------------------------------- mbarrier
 
@@ -143,6 +146,25 @@ __device__ __forceinline__ void red_add_v4_f32(float* dst, float a, float b, flo
                : "memory");
 }
 
+// Asynchronous prefetch of global [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// 16-byte load through the non-coherent path (data not written during the kernel).
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -214,6 +236,59 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same MMA issued by one elected lane of a converged warp. Executed by the
+// whole warp with warp-uniform operands, so the operands stay in uniform
+// registers and consecutive MMAs issue back to back.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One K-chunk of two A tiles (4 K-steps of 16 each, 8 MMAs) issued by one elected
+// lane of a converged warp: D tile j at d_j, A tile j at a + 32 j + 8 kk (TMEM
+// columns), B at b + 2 kk (smem descriptor, 32-byte K steps). The first K step
+// of each tile accumulates only if `accumulate` is non-zero.
+__device__ __forceinline__ void mma_ts_chunk_elect(uint32_t d0, uint32_t d1, uint32_t a,
+                                                   uint64_t b, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+      "add.u32 a4, %2, 32;\n\tadd.u32 a5, %2, 40;\n\tadd.u32 a6, %2, 48;\n\t"
+      "add.u32 a7, %2, 56;\n\t"
+      "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %4, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a4], %3, %4, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a5], b1, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a6], b2, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a7], b3, %4, 1;\n\t}" ::"r"(d0),
+      "r"(d1), "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// mma_commit issued by one elected lane of a converged warp.
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 

@@ -104,10 +104,9 @@ def _pack_reference(qw, scale, bias, kind, F_or_d):
     order = np.array([0, 2, 4, 6, 1, 3, 5, 7])
     perm = np.bitwise_or.reduce(nib[..., order] << (4 * np.arange(8, dtype=np.uint32)), axis=-1)
     perm = perm.astype(np.uint32)
-    sw = ((L >> 2) & 1)[..., None]
-    halves = perm.reshape(*perm.shape[:-1], 2, 4)
-    stored = np.where(sw[..., None] == 1, halves[..., ::-1, :], halves)             # [..., 2, 4]
-    codes = stored.reshape(E, units, nch, 2, 128, 8).astype("<u4").view(np.uint8)
+    halves = perm.reshape(E, units, nch, 2, 128, 2, 4)                              # [.., tile, row, half, 4]
+    stored = halves.transpose(0, 1, 2, 3, 5, 4, 6)                                  # [.., tile, half, row, 4]
+    codes = np.ascontiguousarray(stored).astype("<u4").view(np.uint8)
     codes = codes.reshape(E, units, nch, 2 * 128 * 32)
     g = row * nch + c
     sb = scale.reshape(E, -1)[e, g].astype(np.uint32) | (bias.reshape(E, -1)[e, g].astype(np.uint32) << 16)
