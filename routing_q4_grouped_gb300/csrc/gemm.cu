@@ -42,10 +42,13 @@
 //   epilogue thread gate and up values of one feature and two tokens:
 //   act = bf16(silu(gate) * up), staged in shared memory, written by TMA tile
 //   stores into the tile-padded activation rows. This pass zeroes y_acc.
-// Pass 1 (down): A tile j covers 128 output features; the epilogue scales token
-//   columns by their routing weight (1 for the shared expert), turns each warp's
-//   32 x 32 block around in shared memory and adds it into y_acc with 16-byte
-//   vector reductions (red.global.add.v4.f32).
+// Pass 1 (down): A tile j covers 128 output features; the epilogue moves both
+//   accumulators into a token-major staging area in shared memory and releases
+//   them, then scales each token's 256 outputs (1 KB, contiguous in y_acc) by
+//   its routing weight (1 for the shared expert) and adds them with 16-byte
+//   vector reductions (red.global.add.v4.f32), so the reductions of one unit
+//   overlap the MMAs of the next.
+#include <algorithm>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -61,7 +64,7 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kNMax = 128;                 // rows per unit (MMA N)
 constexpr int kStages = 4;                 // chunk stages of dequantised weights in TMEM
-constexpr int kBSlots = 4;                 // pair slots of token rows in shared memory
+constexpr int kBSlotsMax = 4;              // pair slots of token rows in shared memory (pass 0)
 constexpr int kACols = 64;                 // TMEM columns per chunk stage (2 tiles x 32)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator of tile j at column 256 + 128 j
@@ -78,14 +81,12 @@ static_assert(kThreads == kGemmThreads, "thread count");
 
 constexpr int kBBytes = kNMax * 128;       // token rows of one K-chunk: 64 bf16 (128 B) each, 128B swizzle
 constexpr int kSlotBytes = 2 * kBBytes;    // a pair of K-chunks
-constexpr int kEpiBytes = 32768;           // pass 0: 2 act tiles [128][64] bf16; pass 1: 4 x [32][32] fp32
 constexpr size_t kOffB = 0;
-constexpr size_t kOffEpi = kOffB + size_t(kBSlots) * kSlotBytes;
-constexpr size_t kOffCtl = kOffEpi + kEpiBytes;
+constexpr int kStageRow = 256;             // pass 1 staging: fp32 outputs of a unit per token row
 
 struct Ctl {
-  uint64_t b_full[kBSlots];   // token-row slot landed (transaction bytes)
-  uint64_t b_empty[kBSlots];  // token-row slot's MMAs retired (both MMA warps)
+  uint64_t b_full[kBSlotsMax];   // token-row slot landed (transaction bytes)
+  uint64_t b_empty[kBSlotsMax];  // token-row slot's MMAs retired (both MMA warps)
   uint64_t ready[kStages];    // chunk stage written by its dequant group
   uint64_t consumed[kStages]; // chunk stage's MMAs retired
   uint64_t d_full;            // both MMA warps committed the unit
@@ -100,7 +101,20 @@ struct Ctl {
   float e_w[2][kNMax];    // epilogue (pass 1): routing weight of each row
 };
 
-constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Ctl);
+// Shared memory of each pass. Pass 0: four token-row pair slots and two bf16
+// activation tiles for the TMA stores. Pass 1: two token-row pair slots (tile
+// loads of L2-resident activations need less lookahead than gathers) and a
+// [128 tokens][256 features] fp32 staging area that takes a unit's outputs out
+// of tensor memory, so the accumulators are released before the reductions run.
+template <int MODE>
+struct Layout {
+  static constexpr int kBSlots = MODE == 0 ? 4 : 2;
+  static constexpr size_t kEpi = MODE == 0 ? 32768 : size_t(kNMax) * kStageRow * 4;
+  static constexpr size_t kOffEpi = kOffB + size_t(kBSlots) * kSlotBytes;
+  static constexpr size_t kOffCtl = kOffEpi + kEpi;
+  static constexpr size_t kSmem = 1024 + kOffCtl + sizeof(Ctl);
+};
+static_assert(Layout<1>::kSmem <= 227 * 1024 && Layout<0>::kSmem <= 227 * 1024, "shared memory");
 
 struct Unit {
   int e, row0, rows, p, K;
@@ -160,9 +174,13 @@ __device__ __forceinline__ bool epi_sync(Ctl& ctl, uint32_t& phase, uint64_t lim
 
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-__device__ __forceinline__ uint16_t bf16_bits(float v) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+// (lo, hi) -> bf16x2 bits, each rounded to nearest even, lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
+
 
 // Next (unit, pair) of this CTA's sequence; u starts at blockIdx.x - gridDim.x
 // with pi == npair == 0. Returns false when the sequence is exhausted.
@@ -227,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sB = smem + kOffB;
-  uint8_t* sEpi = smem + kOffEpi;
-  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
+  constexpr int kBSlots = Layout<MODE>::kBSlots;
+  uint8_t* sEpi = smem + Layout<MODE>::kOffEpi;
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + Layout<MODE>::kOffCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -386,12 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = bdesc0 + static_cast<uint64_t>(bs) * (kSlotBytes >> 4);
           mma_ts_chunk_elect(tmem + kDCol, tmem + kDCol + 128, tmem + st * kACols, bd, idesc,
                              (pi | me) != 0);
-          mma_commit_elect(&ctl.consumed[st]);
-          mma_commit_elect(&ctl.b_empty[bs]);
         } else if (lane == 0) {
           raise_abort(ctl, a.err);
         }
+        // hand over first: a commit tracks only this warp's own MMAs
         if (c + 1 < n_chunks) named_bar_arrive(kHandoffBar0 + (me ^ 1u), 64);
+        if (ok) {
+          mma_commit_elect(&ctl.consumed[st]);
+          mma_commit_elect(&ctl.b_empty[bs]);
+        }
       }
       // each warp's commit covers its own MMAs; both together the whole unit
       if (ok) mma_commit_elect(&ctl.d_full);
@@ -470,6 +492,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (size_t i = static_cast<size_t>(blockIdx.x) * (kEpiWarps * 32) + et; i < n4; i += step)
         y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // pass 1: token and routing weight of row et of a unit (shared expert: weight
+    // 1), fetched one unit ahead so the dependent loads overlap the MMAs
+    auto row_info = [&](const Unit& V, int& tt, float& wv) {
+      tt = -1;
+      wv = 0.f;
+      if (et < V.rows) {
+        if (V.shared) {
+          tt = V.row0 + et;
+          wv = 1.f;
+        } else {
+          const int pr = __ldg(a.perm + V.row0 + et);
+          tt = pr / a.k;
+          wv = __ldg(a.wts + pr);
+        }
+      }
+    };
+    auto prefetch_rows = [&](int from, int& tt, float& wv) {
+      for (int v = from; v < total; v += gridDim.x) {
+        Unit V;
+        if (decode_unit(a, n_rt, v, V)) {
+          row_info(V, tt, wv);
+          return;
+        }
+      }
+    };
+    int n_tt = -1;
+    float n_wv = 0.f;
+    if (MODE == 1) prefetch_rows(blockIdx.x, n_tt, n_wv);
     uint32_t nu = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       Unit U;
@@ -477,21 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npad = (U.rows + 15) & ~15;
       const uint32_t db = nu & 1u;
       if (MODE == 1) {
-        // token and weight of each row of the tile (shared expert: weight 1)
-        int tt = -1;
-        float wv = 0.f;
-        if (et < U.rows) {
-          if (U.shared) {
-            tt = U.row0 + et;
-            wv = 1.f;
-          } else {
-            const int pr = __ldg(a.perm + U.row0 + et);
-            tt = pr / a.k;
-            wv = __ldg(a.wts + pr);
-          }
-        }
-        ctl.e_tok[db][et] = tt;
-        ctl.e_w[db][et] = wv;
+        ctl.e_tok[db][et] = n_tt;
+        ctl.e_w[db][et] = n_wv;
+        prefetch_rows(u + gridDim.x, n_tt, n_wv);
       } else {
         // the previous unit's activation stores must have finished reading the staging tiles
         if (q == 0) bulk_wait_read<0>();
@@ -506,32 +544,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lanes 32q..32q+15 hold features 16q..16q+7 of the tile (gate, then up 8 lanes
         // later), lanes 32q+16.. features 16q+8..16q+15
         const int t4 = lane >> 2, tc = 2 * (lane & 3);
-        for (int jt = 0; jt < 2; ++jt) {
-          uint8_t* stile = sEpi + jt * 16384;
-          for (int cc = 0; cc * 32 < npad; ++cc) {
+        // 128B-swizzled staging offset of (token, feature): token * 128 + (16-byte
+        // chunk ^ (token & 7)) * 16 + byte; within a 32-token block token & 7 only
+        // depends on tc + e2, so each (half, e2) has one fixed in-row offset
+        uint32_t inrow[2][2];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t r[16];
-              tmem_ld_16x256b_x4(taddr_q + (static_cast<uint32_t>(half * 16) << 16) + kDCol +
-                                     128 * jt + cc * 32,
-                                 r);
-              tmem_ld_wait();
-              const int fl = 16 * q + 8 * half + t4;          // feature within the tile
+        for (int half = 0; half < 2; ++half)
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                  const int tok = cc * 32 + 8 * jj + tc + e2;  // row within the tile
-                  const float g = __uint_as_float(r[4 * jj + e2]);
-                  const float up = __uint_as_float(r[4 * jj + 2 + e2]);
-                  const uint32_t off =
-                      tok * 128 + ((((fl * 2) >> 4) ^ (tok & 7)) << 4) + ((fl * 2) & 15);
-                  *reinterpret_cast<uint16_t*>(stile + off) = bf16_bits(silu_f(g) * up);
-                }
-              }
-            }
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int fl = 16 * q + 8 * half + t4;            // feature within the tile
+            inrow[half][e2] = ((((fl * 2) >> 4) ^ ((tc + e2) & 7)) << 4) + ((fl * 2) & 15);
           }
-          tc_fence_before();
+        // Load steps in order (tile jt, 32-column block cc, lane half 0 then 1);
+        // the load of the next step is in flight while this one is computed.
+        const int ncc = (npad + 31) / 32;                  // 32-column blocks covering npad
+        const uint32_t hoff = 16u << 16;                   // second half of the lane quarter
+        auto put = [&](const uint32_t (&r)[16], uint8_t* srow, int half) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            // rows 8 jj + tc and 8 jj + tc + 1 of the block: one packed conversion
+            const float a0 = silu_f(__uint_as_float(r[4 * jj])) * __uint_as_float(r[4 * jj + 2]);
+            const float a1 =
+                silu_f(__uint_as_float(r[4 * jj + 1])) * __uint_as_float(r[4 * jj + 3]);
+            const uint32_t p = bf16x2_bits(a0, a1);
+            *reinterpret_cast<uint16_t*>(srow + (8 * jj) * 128 + inrow[half][0]) =
+                static_cast<uint16_t>(p & 0xFFFFu);
+            *reinterpret_cast<uint16_t*>(srow + (8 * jj + 1) * 128 + inrow[half][1]) =
+                static_cast<uint16_t>(p >> 16);
+          }
+        };
+        uint32_t ra[16], rb[16];
+        tmem_ld_16x256b_x4(taddr_q + kDCol, ra);
+        for (int jt = 0; jt < 2; ++jt) {
+          for (int cc = 0; cc < ncc; ++cc) {
+            const uint32_t col = taddr_q + kDCol + 128 * jt + 32 * cc;
+            uint8_t* srow = sEpi + jt * 16384 + tc * 128 + cc * 32 * 128;
+            tmem_ld_wait();
+            tmem_regs_ready(ra);
+            tmem_ld_16x256b_x4(col + hoff, rb);
+            put(ra, srow, 0);
+            tmem_ld_wait();
+            tmem_regs_ready(rb);
+            const bool last = cc + 1 == ncc;
+            if (!last)
+              tmem_ld_16x256b_x4(col + 32, ra);
+            else if (jt == 0)
+              tmem_ld_16x256b_x4(taddr_q + kDCol + 128, ra);
+            put(rb, srow, 1);
+          }
+          tc_fence_before();                                // accumulator jt fully read
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.d_empty[jt]);
         }
@@ -550,40 +611,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit();
         }
       } else {
-        // warp-private transpose through shared memory: lane = output feature in
-        // TMEM, then lane = 4 consecutive features of one token for a 16-byte reduction
-        float* st = reinterpret_cast<float*>(sEpi) + q * 32 * 32;
-        const int rsub = lane >> 3, c4 = 4 * (lane & 7);
+        // Move both accumulators into the token-major staging rows and release
+        // them at once; the next unit's MMAs start while this unit's rows are
+        // scaled by their routing weight and added into y_acc, one asynchronous
+        // 1 KB bulk reduction per token row.
+        float* stg = reinterpret_cast<float*>(sEpi);
         for (int jt = 0; jt < 2; ++jt) {
-          const int col0 = 256 * U.p + 128 * jt + 32 * q;   // this warp's first output feature
+          float* col = stg + 128 * jt + 32 * q + lane;       // this thread's feature column
           for (int cc = 0; cc * 32 < npad; ++cc) {
             uint32_t dv[32];
             tmem_ld_32x32b_x32(taddr_q + kDCol + 128 * jt + cc * 32, dv);
-            tmem_ld_wait();
-            __syncwarp();
+            tmem_ld_wait();   // only stores (ordered by the wait's memory clobber) follow
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              st[jj * 32 + lane] = __uint_as_float(dv[jj]) * ctl.e_w[db][cc * 32 + jj];
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int row = 4 * i + rsub;                 // token column within the chunk
-              const int tj = ctl.e_tok[db][cc * 32 + row];
-              if (cc * 32 + row < U.rows && tj >= 0) {
-                const float4 v = *reinterpret_cast<const float4*>(st + row * 32 + c4);
-                red_add_v4_f32(a.y_acc + static_cast<size_t>(tj) * a.d + col0 + c4, v.x, v.y, v.z,
-                               v.w);
-              }
-            }
+            for (int jj = 0; jj < 32; ++jj) col[(cc * 32 + jj) * kStageRow] = __uint_as_float(dv[jj]);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.d_empty[jt]);
         }
+        if (!epi_sync(ctl, gs_phase, lim)) {   // every feature column of the staging rows written
+          if (lane == 0) raise_abort(ctl, a.err);
+          break;
+        }
+        // warp q adds rows q, q+4, ...: each lane scales two 16-byte words of the
+        // row and adds them with vector reductions (512 contiguous bytes per
+        // warp instruction)
+        for (int row = q; row < U.rows; row += kEpiWarps) {
+          const int tj = ctl.e_tok[db][row];
+          if (tj < 0) continue;
+          const float w = ctl.e_w[db][row];
+          const float4* rp = reinterpret_cast<const float4*>(stg + row * kStageRow);
+          float* dst = a.y_acc + static_cast<size_t>(tj) * a.d + 256 * U.p + 4 * lane;
+          const float4 v0 = rp[lane], v1 = rp[32 + lane];
+          red_add_v4_f32(dst, v0.x * w, v0.y * w, v0.z * w, v0.w * w);
+          red_add_v4_f32(dst + 128, v1.x * w, v1.y * w, v1.z * w, v1.w * w);
+        }
       }
       ++nu;
     }
-    if (q == 0) bulk_wait<0>();   // outstanding stores / reductions complete before exit
+    bulk_wait<0>();   // outstanding stores / reductions complete before exit
   }
 
   __syncthreads();
@@ -619,11 +685,12 @@ cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& m, int grid, cudaStre
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(q4_grouped_gemm_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+                                         static_cast<int>(Layout<MODE>::kSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  q4_grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(m.B, m.B_sh, m.C, m.C_sh, a);
+  q4_grouped_gemm_kernel<MODE><<<grid, kThreads, Layout<MODE>::kSmem, s>>>(m.B, m.B_sh, m.C, m.C_sh,
+                                                                         a);
   return cudaGetLastError();
 }
 
@@ -650,7 +717,7 @@ FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles) {
 
 int gemm_tile_rows() { return kNMax; }
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
+size_t gemm_smem_bytes() { return std::max(Layout<0>::kSmem, Layout<1>::kSmem); }
 
 cudaError_t launch_gemm(int mode, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s) {
   if (mode == 0) return launch_mode<0>(a, m, grid, s);
