@@ -25,22 +25,97 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Status and count share one 32-bit word, so a relaxed load sees a consistent
+// pair; relaxed loads of different words may be in flight together, where
+// acquire loads would wait for one another.
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-// (v1, e1) ranks before (v2, e2): larger logit first, equal logits by lower index.
-__device__ __forceinline__ bool ranks_before(float v1, int e1, float v2, int e2) {
-  return v1 > v2 || (v1 == v2 && e1 < e2);
+// Order-preserving unsigned key of a non-NaN float (larger float, larger key;
+// -inf maps to 0x007FFFFF, so 0 can mark "no candidate").
+__device__ __forceinline__ uint32_t float_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Keys of the logits of token t (lane holds experts lane + 32 s); 0 where
+// s is out of range or the token is not loaded. NaN counts as -inf and, like
+// +-inf, sets the non-finite error bit.
+template <int S>
+__device__ __forceinline__ void load_keys(const RouteArgs& a, int t, bool tok, int lane,
+                                          uint32_t (&key)[S]) {
+  const float* row = a.logits + static_cast<size_t>(tok ? t : 0) * a.E;
+  bool bad = false;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int e = lane + 32 * s;
+    uint32_t kk = 0;
+    if (tok && e < a.E) {
+      float x = __ldg(row + e);
+      if (!isfinite(x)) {
+        bad = true;
+        if (isnan(x)) x = -INFINITY;
+      }
+      kk = float_key(x);
+    }
+    key[s] = kk;
+  }
+  if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
+}
+
+// Top-k of one token's keys: rank j is the largest remaining key, the lowest
+// expert index among equal keys (two warp reductions per rank). Choice j ends
+// in lane sp * kp + j as (pv, pe).
+template <int S>
+__device__ __forceinline__ void select_topk(const uint32_t (&key)[S], int k, int kp, int sp,
+                                            int lane, float& pv, int& pe) {
+  int my_e = 0;
+  uint32_t my_k = 0;
+  uint32_t taken = 0;                  // bit s: key[s] of this lane already chosen
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0;
+    int bs = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {        // ascending s: equal keys keep the lower index
+      const uint32_t ks = ((taken >> s) & 1u) ? 0u : key[s];
+      if (ks > bk) {
+        bk = ks;
+        bs = s;
+      }
+    }
+    const uint32_t wk = __reduce_max_sync(kFull, bk);
+    const uint32_t we =
+        __reduce_min_sync(kFull, bk == wk ? static_cast<uint32_t>(lane + 32 * bs) : 0xFFFFFFFFu);
+    if (static_cast<int>(we & 31u) == lane) taken |= 1u << (we >> 5);
+    if (lane == j) {
+      my_e = static_cast<int>(we);
+      my_k = wk;
+    }
+  }
+  const uint32_t sk = __shfl_sync(kFull, my_k, lane % kp);
+  const int se = __shfl_sync(kFull, my_e, lane % kp);
+  if (lane / kp == sp) {
+    pv = key_float(sk);
+    pe = se;
+  }
 }
 
 // Kernel 1: selection, histogram with stable local ranks, lookback prefix,
 // and (in the last block to finish) counts, offsets and the block map.
 // S = logits held per lane (E <= 32 * S). One warp handles one token at a time.
 template <int S>
-__global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const RouteArgs a) {
+__global__ void __launch_bounds__(kRouteThreads, 1) route_select_kernel(const RouteArgs a) {
   extern __shared__ int smem[];
   __shared__ int s_b, s_last;
   __shared__ int s_wsum[2][kRouteThreads / 32];
@@ -61,67 +136,45 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
   const int t0 = b * kRouteTokensPerBlock;
   const int nt = max(0, min(kRouteTokensPerBlock, a.T - t0));
 
-  // ---- per-token top-k on the fp32 logits + weights
-  for (int i = warp; i < nt; i += kRouteThreads / 32) {
-    const int t = t0 + i;
-    const float* row = a.logits + static_cast<size_t>(t) * E;
-    float v[S];
-    bool bad = false;
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-      const int e = lane + 32 * s;
-      float x = -INFINITY;
-      if (e < E) {
-        x = __ldg(row + e);
-        if (!isfinite(x)) {
-          bad = true;
-          if (isnan(x)) x = -INFINITY;
-        }
-      }
-      v[s] = x;
+  // ---- per-token top-k on the fp32 logits, then the weights for up to P tokens
+  // at once: the fp64 pipe is narrow, so the k choices of P = 32 / kp tokens
+  // (kp = k rounded up to a power of two) share one pass of fp64 instructions,
+  // token s of the pack in lanes [s kp, s kp + k). The logit rows of a pack are
+  // loaded together; each rank is found with two warp reductions, the largest
+  // order-preserving key of the logit, then the lowest expert index among ties.
+  const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
+  const int P = 32 / kp;
+  constexpr int kWarps = kRouteThreads / 32;
+  constexpr int kPackMax = 4;         // rows held in registers at a time (P may be larger)
+  for (int i0 = warp; i0 < nt; i0 += kWarps * P) {
+    float pv = -INFINITY;             // this lane's packed choice (token lane / kp, rank lane % kp)
+    int pe = 0;
+    for (int sb = 0; sb < P; sb += kPackMax) {
+      // keys of the pack's (up to) four rows, 0 = not a candidate
+      uint32_t k0[S], k1[S], k2[S], k3[S];
+      auto row_ok = [&](int q) { return sb + q < P && i0 + kWarps * (sb + q) < nt; };
+      load_keys<S>(a, t0 + i0 + kWarps * sb, row_ok(0), lane, k0);
+      load_keys<S>(a, t0 + i0 + kWarps * (sb + 1), row_ok(1), lane, k1);
+      load_keys<S>(a, t0 + i0 + kWarps * (sb + 2), row_ok(2), lane, k2);
+      load_keys<S>(a, t0 + i0 + kWarps * (sb + 3), row_ok(3), lane, k3);
+      if (row_ok(0)) select_topk<S>(k0, k, kp, sb + 0, lane, pv, pe);
+      if (row_ok(1)) select_topk<S>(k1, k, kp, sb + 1, lane, pv, pe);
+      if (row_ok(2)) select_topk<S>(k2, k, kp, sb + 2, lane, pv, pe);
+      if (row_ok(3)) select_topk<S>(k3, k, kp, sb + 3, lane, pv, pe);
     }
-    if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
-
-    uint32_t used = 0;
-    int my_e = 0;
-    float my_v = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int s = 0; s < S; ++s) {
-        const int e = lane + 32 * s;
-        if (e < E && !((used >> s) & 1u) && ranks_before(v[s], e, bv, be)) {
-          bv = v[s];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oe = __shfl_xor_sync(kFull, be, off);
-        if (ranks_before(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) used |= 1u << (be >> 5);
-      if (lane == j) {
-        my_e = be;
-        my_v = bv;
-      }
-    }
-    // renormalised softmax over the chosen experts: exp(l_j - l_max) / sum, in fp64
-    const float m = __shfl_sync(kFull, my_v, 0);
-    double ex = (lane < k) ? exp(static_cast<double>(my_v) - static_cast<double>(m)) : 0.0;
+    // renormalised softmax over each token's choices: exp(l_j - l_max) / sum, in fp64
+    const int sp = lane / kp, j = lane % kp;
+    const int i = i0 + kWarps * sp;
+    const bool act = j < k && i < nt;
+    const float m = __shfl_sync(kFull, pv, sp * kp);   // the token's top logit (rank 0)
+    double ex = act ? exp(static_cast<double>(pv) - static_cast<double>(m)) : 0.0;
     double sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < k) {
-      const size_t o = static_cast<size_t>(t) * k + lane;
-      a.ids[o] = my_e;
+    for (int off = kp >> 1; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (act) {
+      const size_t o = static_cast<size_t>(t0 + i) * k + j;
+      a.ids[o] = pe;
       a.w[o] = static_cast<float>(ex / sum);
-      sE[i * k + lane] = my_e;
+      sE[i * k + j] = pe;
     }
   }
   __syncthreads();
@@ -168,7 +221,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
         uint32_t word[kLookback];
 #pragma unroll
         for (int i = 0; i < kLookback; ++i)
-          word[i] = (p - i >= 0) ? ld_acquire(a.lb + static_cast<size_t>(p - i) * E + e) : kLbInclusive;
+          word[i] = (p - i >= 0) ? ld_relaxed(a.lb + static_cast<size_t>(p - i) * E + e) : kLbInclusive;
         int used = 0;
 #pragma unroll
         for (int i = 0; i < kLookback; ++i) {
