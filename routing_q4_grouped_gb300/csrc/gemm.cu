@@ -12,29 +12,31 @@
 // into tensor memory (tcgen05.st) as the MMA's A operand: no bf16 weight tile
 // touches shared or global memory.
 //
-// The pipeline advances in pairs of K-chunks (K = 128), so every barrier wait is
-// paid once per two quantisation groups:
-//   packed weights  read by the dequant warps themselves, one pair ahead, with
-//                   16-byte loads (each warp load covers 512 contiguous bytes);
-//                   an L2 bulk prefetch of the next unit's blocks hides HBM latency
+// Data movement:
+//   packed weights  read by the dequant warps themselves, one pair of K-chunks
+//                   ahead, with 16-byte loads (each warp load covers 512
+//                   contiguous bytes); an L2 bulk prefetch of the next unit's
+//                   blocks hides HBM latency
 //   token rows      gate/up pass: gather4 of x rows; down pass: 16-row tiles of
-//                   the tile-padded activation rows; issued by seven warps
-// A pair slot (2 of them) joins the pair's token rows in shared memory with its
-// A stage in tensor memory: a `ready` barrier collects the sixteen dequant warps,
-// a `consumed` commit frees the stage; token rows have a deeper ring of their own.
+//                   the tile-padded activation rows; a ring of pair slots (K =
+//                   128) filled by six producer warps
+// Dequantised weights go into four chunk stages in tensor memory: a `ready`
+// barrier collects the eight dequant warps of the chunk's parity group (and,
+// through that group's first warp, the pair's token rows), a `consumed` barrier
+// takes one commit from each MMA warp and frees the stage.
 //
 // Warp roles (896 threads, one CTA per SM, persistent over units):
 //   warps 0-15   dequantisation: warp w expands chunk w/8 of every pair for A
 //                tile (w/4)%2, TMEM lane quarter w%4
 //   warps 16-19  epilogue, lane quarter w-16
-//   warps 20-26  producers of token rows (warp 20 also prefetches weights into L2)
-//   warp 27      TMEM allocator and MMA issuer: the whole warp runs the loop with
-//                warp-uniform operands and one elected lane issues each MMA, which
-//                keeps the tensor pipe fed back to back
-// Tensor memory: columns [0, 256) hold 2 pair stages of 128 columns (tile j,
-// chunk h of the pair at 64 j + 32 h), [256, 512) the two accumulators (A tile
-// j -> 256 + 128 j). An accumulator is released as soon as the epilogue has read
-// it, so the next unit's MMAs on tile 0 overlap the epilogue of tile 1.
+//   warps 20-25  producers of token rows (warp 20 also prefetches weights into L2)
+//   warps 26-27  MMA issuers (26 also allocates tensor memory): warp 26 + j
+//                issues every chunk's MMAs of A tile j into accumulator j; the
+//                two run in parallel, each as a whole warp with warp-uniform
+//                operands and one elected lane issuing
+// Tensor memory: columns [0, 256) hold 4 chunk stages of 64 columns (tile j at
+// +32 j), [256, 512) the two accumulators (A tile j -> 256 + 128 j), each
+// released as soon as the epilogue has read it.
 //
 // Pass 0 (gate/up): A tile j covers 64 output features with gate and up rows
 //   interleaved in blocks of 8 (TMEM lanes 16m..16m+7 = gate rows of features
@@ -74,9 +76,8 @@ constexpr int kEpiWarp0 = 16;              // warp % 4 = TMEM lane quarter
 constexpr int kEpiWarps = 4;
 constexpr int kProdWarp0 = 20;
 constexpr int kProdWarps = 6;
-constexpr int kMmaWarp0 = 26;              // two MMA issuers: warp 26 + chunk parity
+constexpr int kMmaWarp0 = 26;              // two MMA issuers: warp 26 + A tile
 constexpr int kThreads = 28 * 32;
-constexpr uint32_t kHandoffBar0 = 1;       // named barriers 1, 2: MMA issue order handoff
 static_assert(kThreads == kGemmThreads, "thread count");
 
 constexpr int kBBytes = kNMax * 128;       // token rows of one K-chunk: 64 bf16 (128 B) each, 128B swizzle
@@ -253,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kBSlots; ++s) {
       mbar_init(&ctl.b_full[s], 1);
-      mbar_init(&ctl.b_empty[s], 2);
+      mbar_init(&ctl.b_empty[s], 2);    // one commit per MMA warp
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl.ready[s], kDqGroupWarps);
-      mbar_init(&ctl.consumed[s], 1);
+      mbar_init(&ctl.consumed[s], 2);   // one commit per MMA warp
     }
     mbar_init(&ctl.d_full, 2);
     mbar_init(&ctl.drain2, 1);
@@ -367,60 +368,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kMmaWarp0) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp kMmaWarp0 + m issues chunk m of every pair, so chunks alternate
-    // between the two warps in K order: before chunk c it waits on named
-    // barrier kHandoffBar0 + m, which the other warp arrives at once it has
-    // issued chunk c-1. One warp's barrier waits thus overlap the other's MMAs.
-    // Each warp runs the loop with warp-uniform operands and one elected lane
-    // issues. Both warps walk the same pair sequence to its end, also after an
-    // abort, so every handoff is matched.
-    const uint32_t me = static_cast<uint32_t>(warp - kMmaWarp0);
-    uint32_t n_chunks = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      Unit U;
-      if (decode_unit(a, n_rt, u, U)) n_chunks += U.K / 64;
-    }
+    // Warp kMmaWarp0 + j owns A tile j and its accumulator: per chunk it waits
+    // for the stage, issues the tile's 4 MMAs and commits. The two warps run in
+    // parallel on the same stages; each accumulator sees a single issuing warp,
+    // so the K order within it needs no handoff. The whole warp runs the loop
+    // with warp-uniform operands and one elected lane issues.
+    const uint32_t j = static_cast<uint32_t>(warp - kMmaWarp0);
     uint32_t ip = 0, nu = 0;
     bool ok = true;
-    const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB)) + me * (kBBytes >> 4);
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
+    const uint32_t dcol = tmem + kDCol + 128 * j;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
       if (!decode_unit(a, n_rt, u, U)) continue;
       const uint32_t npad = (U.rows + 15) & ~15;
       const uint32_t idesc = idesc_bf16_f32(128, npad);
       const int npair = U.K / 128;
-      for (int pi = 0; pi < npair; ++pi, ++ip) {
-        const uint32_t c = 2 * ip + me;                 // chunk index in the CTA's sequence
+      for (int pi = 0; pi < npair && ok; ++pi, ++ip) {
         const uint32_t bs = ip % kBSlots;
-        const uint32_t st = c % kStages;
-        // ready[st] also covers the pair's token rows (see the dequant warps)
-        if (ok) ok = __all_sync(kFull, mbar_wait(&ctl.ready[st], (c / kStages) & 1u, abortp, lim));
-        if (ok && pi == 0 && me == 0) {   // the epilogue must have drained both accumulators
-          ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[0], (nu & 1u) ^ 1u, abortp, lim)) &&
-               __all_sync(kFull, mbar_wait(&ctl.d_empty[1], (nu & 1u) ^ 1u, abortp, lim));
-        }
-        if (c > 0) named_bar_sync(kHandoffBar0 + me, 64);   // chunk c-1 has been issued
-        if (ok) {
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>(bs) * (kSlotBytes >> 4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t c = 2 * ip + h;                  // chunk index in the CTA's sequence
+          const uint32_t st = c % kStages;
+          // ready[st] also covers the pair's token rows (see the dequant warps)
+          ok = ok && __all_sync(kFull, mbar_wait(&ctl.ready[st], (c / kStages) & 1u, abortp, lim));
+          if (ok && pi == 0 && h == 0)   // the epilogue must have read this accumulator
+            ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[j], (nu & 1u) ^ 1u, abortp, lim));
+          if (!ok) break;
           tc_fence_after();
-          const uint64_t bd = bdesc0 + static_cast<uint64_t>(bs) * (kSlotBytes >> 4);
-          mma_ts_chunk_elect(tmem + kDCol, tmem + kDCol + 128, tmem + st * kACols, bd, idesc,
-                             (pi | me) != 0);
-        } else if (lane == 0) {
-          raise_abort(ctl, a.err);
-        }
-        // hand over first: a commit tracks only this warp's own MMAs
-        if (c + 1 < n_chunks) named_bar_arrive(kHandoffBar0 + (me ^ 1u), 64);
-        if (ok) {
+          mma_ts_tile_chunk_elect(dcol, tmem + st * kACols + 32 * j, bd + h * (kBBytes >> 4), idesc,
+                                  (pi | h) != 0);
           mma_commit_elect(&ctl.consumed[st]);
-          mma_commit_elect(&ctl.b_empty[bs]);
         }
+        if (ok) mma_commit_elect(&ctl.b_empty[bs]);
       }
-      // each warp's commit covers its own MMAs; both together the whole unit
       if (ok) mma_commit_elect(&ctl.d_full);
       ++nu;
     }
+    if (!ok && lane == 0) raise_abort(ctl, a.err);
     // every issued MMA must retire before tensor memory is released
-    uint64_t* dr = me ? &ctl.drain2 : &ctl.drain;
+    uint64_t* dr = j ? &ctl.drain2 : &ctl.drain;
     mma_commit_elect(dr);
     mbar_wait(dr, 0, &ctl.zero, lim);
     __syncwarp();

@@ -284,6 +284,28 @@ __device__ __forceinline__ void mma_ts_chunk_elect(uint32_t d0, uint32_t d1, uin
       : "memory");
 }
 
+// One K-chunk of one A tile (4 K-steps of 16, 4 MMAs) issued by one elected lane
+// of a converged warp: A at a + 8 kk (TMEM columns), B at b + 2 kk (smem
+// descriptor, 32-byte K steps). The first K step accumulates only if
+// `accumulate` is non-zero.
+__device__ __forceinline__ void mma_ts_tile_chunk_elect(uint32_t d, uint32_t a, uint64_t b,
+                                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      ".reg .b32 a1, a2, a3;\n\t"
+      ".reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, 1;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // mma_commit issued by one elected lane of a converged warp.
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
