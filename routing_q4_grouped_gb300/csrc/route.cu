@@ -331,9 +331,20 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const RouteArgs a) {
     const int e = a.ids[i];
     const int t = static_cast<int>(i / a.k);
     const int b = t / kRouteTokensPerBlock;
-    const int pos = a.offsets[e] + a.blk_base[static_cast<size_t>(b) * a.E + e] + a.lrank[i];
+    // after a failed selection (error word set) the inputs here may be partial:
+    // never write outside perm
+    if (e < 0 || e >= a.E) {
+      atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);
+      continue;
+    }
+    const long long pos = static_cast<long long>(a.offsets[e]) +
+                          a.blk_base[static_cast<size_t>(b) * a.E + e] + a.lrank[i];
+    if (pos < 0 || pos >= static_cast<long long>(n)) {
+      atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);
+      continue;
+    }
     a.perm[pos] = static_cast<int32_t>(i);
-    a.inv[i] = pos;
+    a.inv[i] = static_cast<int32_t>(pos);
   }
   const size_t nlb = static_cast<size_t>(a.nblk) * a.E;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < nlb; i += stride)
