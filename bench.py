@@ -77,10 +77,14 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
-    if that summary was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"gemm_gate_up_{workload}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary
+    of this workload (the gate/up kernel's own summary, else the summary of all
+    the layer's kernels), if it was taken on the current kernel sources (else None)."""
+    for name in (f"gemm_gate_up_{workload}.md", f"layer_kernels_{workload}.md"):
+        path = os.path.join(ROOT, "profiles", name)
+        if os.path.exists(path):
+            break
+    else:
         return None
     txt = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
