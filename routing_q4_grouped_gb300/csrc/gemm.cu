@@ -20,23 +20,26 @@
 //   token rows      gate/up pass: gather4 of x rows; down pass: 16-row tiles of
 //                   the tile-padded activation rows; a ring of pair slots (K =
 //                   128) filled by six producer warps
-// Dequantised weights go into four chunk stages in tensor memory: a `ready`
-// barrier collects the eight dequant warps of the chunk's parity group (and,
-// through that group's first warp, the pair's token rows), a `consumed` barrier
-// takes one commit from each MMA warp and frees the stage.
+// Dequantised weights go into two pair stages in tensor memory (a K-pair of two
+// 64-wide chunks each), one per dequant group: a `ready` barrier collects the
+// group's eight warps, a `consumed` barrier takes one commit from each MMA warp
+// and frees the stage; the MMA warps also wait for the pair's token rows
+// (`b_full`). One barrier round trip per 128 of K keeps the fixed cost per
+// handoff small next to the MMAs even when a unit has only 16 token rows.
 //
 // Warp roles (896 threads, one CTA per SM, persistent over units):
-//   warps 0-15   dequantisation: warp w expands chunk w/8 of every pair for A
-//                tile (w/4)%2, TMEM lane quarter w%4
+//   warps 0-15   dequantisation: warp w expands both chunks of every second
+//                pair (index parity w/8) for A tile (w/4)%2, TMEM lane quarter w%4
 //   warps 16-19  epilogue, lane quarter w-16
 //   warps 20-25  producers of token rows (warp 20 also prefetches weights into L2)
 //   warps 26-27  MMA issuers (26 also allocates tensor memory): warp 26 + j
-//                issues every chunk's MMAs of A tile j into accumulator j; the
+//                issues every pair's 8 MMAs of A tile j into accumulator j; the
 //                two run in parallel, each as a whole warp with warp-uniform
 //                operands and one elected lane issuing
 // Tensor memory: columns [0, 256) hold 4 chunk stages of 64 columns (tile j at
-// +32 j), [256, 512) the two accumulators (A tile j -> 256 + 128 j), each
-// released as soon as the epilogue has read it.
+// +32 j; stages 2s and 2s+1 form pair stage s), [256, 512) the two
+// accumulators (A tile j -> 256 + 128 j), each released as soon as the
+// epilogue has read it.
 //
 // Pass 0 (gate/up): A tile j covers 64 output features with gate and up rows
 //   interleaved in blocks of 8 (TMEM lanes 16m..16m+7 = gate rows of features
@@ -66,12 +69,13 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kNMax = 128;                 // rows per unit (MMA N)
 constexpr int kStages = 4;                 // chunk stages of dequantised weights in TMEM
+constexpr int kPairStages = kStages / 2;   // a K-pair of chunk stages per barrier
 constexpr int kBSlotsMax = 4;              // pair slots of token rows in shared memory (pass 0)
 constexpr int kACols = 64;                 // TMEM columns per chunk stage (2 tiles x 32)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = 256;            // accumulator of tile j at column 256 + 128 j
-constexpr int kDqWarps = 16;               // warp w: chunk w/8 of each pair, A tile (w/4)%2
-constexpr int kDqGroupWarps = 8;           // warps per chunk parity
+constexpr int kDqWarps = 16;               // warp w: pairs of parity w/8, A tile (w/4)%2
+constexpr int kDqGroupWarps = 8;           // warps per pair-parity group
 constexpr int kEpiWarp0 = 16;              // warp % 4 = TMEM lane quarter
 constexpr int kEpiWarps = 4;
 constexpr int kProdWarp0 = 20;
@@ -88,8 +92,8 @@ constexpr int kStageRow = 256;             // pass 1 staging: fp32 outputs of a 
 struct Ctl {
   uint64_t b_full[kBSlotsMax];   // token-row slot landed (transaction bytes)
   uint64_t b_empty[kBSlotsMax];  // token-row slot's MMAs retired (both MMA warps)
-  uint64_t ready[kStages];    // chunk stage written by its dequant group
-  uint64_t consumed[kStages]; // chunk stage's MMAs retired
+  uint64_t ready[kPairStages];    // pair stage written by its dequant group
+  uint64_t consumed[kPairStages]; // pair stage's MMAs retired (both MMA warps)
   uint64_t d_full;            // both MMA warps committed the unit
   uint64_t drain2;
   uint64_t d_empty[2];
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.b_full[s], 1);
       mbar_init(&ctl.b_empty[s], 2);    // one commit per MMA warp
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kPairStages; ++s) {
       mbar_init(&ctl.ready[s], kDqGroupWarps);
       mbar_init(&ctl.consumed[s], 2);   // one commit per MMA warp
     }
@@ -368,11 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kMmaWarp0) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp kMmaWarp0 + j owns A tile j and its accumulator: per chunk it waits
-    // for the stage, issues the tile's 4 MMAs and commits. The two warps run in
-    // parallel on the same stages; each accumulator sees a single issuing warp,
-    // so the K order within it needs no handoff. The whole warp runs the loop
-    // with warp-uniform operands and one elected lane issues.
+    // Warp kMmaWarp0 + j owns A tile j and its accumulator: per K-pair it waits
+    // for the pair stage, issues the tile's 8 MMAs and commits. The two warps
+    // run in parallel on the same stages; each accumulator sees a single
+    // issuing warp, so the K order within it needs no handoff. The whole warp
+    // runs the loop with warp-uniform operands and one elected lane issues.
     const uint32_t j = static_cast<uint32_t>(warp - kMmaWarp0);
     uint32_t ip = 0, nu = 0;
     bool ok = true;
@@ -387,21 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int pi = 0; pi < npair && ok; ++pi, ++ip) {
         const uint32_t bs = ip % kBSlots;
         const uint64_t bd = bdesc0 + static_cast<uint64_t>(bs) * (kSlotBytes >> 4);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t c = 2 * ip + h;                  // chunk index in the CTA's sequence
-          const uint32_t st = c % kStages;
-          // ready[st] also covers the pair's token rows (see the dequant warps)
-          ok = ok && __all_sync(kFull, mbar_wait(&ctl.ready[st], (c / kStages) & 1u, abortp, lim));
-          if (ok && pi == 0 && h == 0)   // the epilogue must have read this accumulator
-            ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[j], (nu & 1u) ^ 1u, abortp, lim));
-          if (!ok) break;
-          tc_fence_after();
-          mma_ts_tile_chunk_elect(dcol, tmem + st * kACols + 32 * j, bd + h * (kBBytes >> 4), idesc,
-                                  (pi | h) != 0);
-          mma_commit_elect(&ctl.consumed[st]);
-        }
-        if (ok) mma_commit_elect(&ctl.b_empty[bs]);
+        const uint32_t ps = ip % kPairStages;
+        ok = __all_sync(kFull, mbar_wait(&ctl.ready[ps], (ip / kPairStages) & 1u, abortp, lim)) &&
+             __all_sync(kFull, mbar_wait(&ctl.b_full[bs], (ip / kBSlots) & 1u, abortp, lim));
+        if (ok && pi == 0)   // the epilogue must have read this accumulator
+          ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[j], (nu & 1u) ^ 1u, abortp, lim));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a0 = tmem + 2 * ps * kACols + 32 * j;
+        mma_ts_tile_pair_elect(dcol, a0, a0 + kACols, bd, bd + (kBBytes >> 4), idesc, pi != 0);
+        mma_commit_elect(&ctl.consumed[ps]);
+        mma_commit_elect(&ctl.b_empty[bs]);
       }
       if (ok) mma_commit_elect(&ctl.d_full);
       ++nu;
@@ -414,55 +414,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kDqWarps) {
     // ------------------------------------------------------ dequantisation
-    // Warp w expands chunk w/8 of every pair for A tile (w/4)%2, TMEM lane
-    // quarter w%4, so the two chunk parities form two groups that run half a
-    // pair apart. The ready barrier of a chunk completes once the group has
-    // stored it and (checked by the group's first warp) its token rows landed. The next pair's chunk is expanded into registers as soon as
-    // the current one is published: once a stage frees, only the tensor-memory
-    // stores stand between the MMAs and the next stage.
+    // Two groups of eight warps take turns: group g = w/8 expands the pairs of
+    // the CTA's sequence whose index has parity g, always into pair stage g;
+    // warp w covers A tile (w/4)%2, TMEM lane quarter w%4, both chunks of the
+    // pair. Each group's ready barrier completes once its eight warps have
+    // stored the pair. The groups run a pair apart, so one group's stores
+    // overlap the other's arithmetic, and a warp's loads of its next pair are
+    // issued as soon as the registers free, two pairs of the sequence ahead.
     const int q = warp & 3;           // TMEM lane quarter
     const int j = (warp >> 2) & 1;    // A tile
-    const int h = warp >> 3;          // chunk within the pair
+    const int g = warp >> 3;          // pair parity
     const int L = q * 32 + lane;      // TMEM lane = A row
-    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j;
-    const uint32_t roff = h * kPackChunkBytes + j * 4096 + L * 16;          // row codes
-    const uint32_t soff = h * kPackChunkBytes + 8192 + (j * 128 + L) * 4;   // scale|bias
+    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j + 2 * g * kACols;
+    const uint32_t roff = j * 4096 + L * 16;          // row codes (chunk h: + h * kPackChunkBytes)
+    const uint32_t soff = 8192 + (j * 128 + L) * 4;   // scale|bias
     int cu = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), cpi = 0, cnp = 0;
     const uint8_t* cbl = nullptr;
+    ChunkWords n0, n1;
     bool have = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
-    ChunkWords n;                     // packed words of this warp's chunk of the next pair
-    if (have) load_chunk(cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes), roff, soff, n);
-    uint32_t ip = 0;
+    if (have && g == 1) have = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+    if (have) {
+      const uint8_t* pb = cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes);
+      load_chunk(pb, roff, soff, n0);
+      load_chunk(pb + kPackChunkBytes, roff, soff, n1);
+    }
+    uint32_t it = 0;
     bool ok = true;
     while (have) {
-      uint32_t v[32];
-      dequant_chunk(n, v);
-      const bool more = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
-      if (more) load_chunk(cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes), roff, soff, n);
-      const uint32_t c = 2 * ip + h;                     // chunk index in the CTA's sequence
-      const uint32_t st = c % kStages;
-      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[st], ((c / kStages) & 1u) ^ 1u, abortp, lim))) {
+      bool more = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+      if (more) more = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+      const uint8_t* pb = more ? cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes) : nullptr;
+      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[g], (it & 1u) ^ 1u, abortp, lim))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t t = tq + st * kACols;
-      tmem_st_32x32b_x16(t, *reinterpret_cast<const uint32_t(*)[16]>(v));
-      tmem_st_32x32b_x16(t + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
+      uint32_t v[32];
+      dequant_chunk(n0, v);
+      if (more) load_chunk(pb, roff, soff, n0);
+      tmem_st_32x32b_x16(tq, *reinterpret_cast<const uint32_t(*)[16]>(v));
+      tmem_st_32x32b_x16(tq + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
+      dequant_chunk(n1, v);
+      if (more) load_chunk(pb + kPackChunkBytes, roff, soff, n1);
+      tmem_st_32x32b_x16(tq + kACols, *reinterpret_cast<const uint32_t(*)[16]>(v));
+      tmem_st_32x32b_x16(tq + kACols + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
       tmem_st_wait();
       tc_fence_before();
-      if ((warp & 7) == 0) {
-        // the first warp of the group also vouches for the pair's token rows, so
-        // the MMA warps wait on a single barrier per chunk
-        const uint32_t bs = ip % kBSlots;
-        if (!__all_sync(kFull, mbar_wait(&ctl.b_full[bs], (ip / kBSlots) & 1u, abortp, lim))) {
-          ok = false;
-          break;
-        }
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.ready[st]);
-      ++ip;
+      if (lane == 0) mbar_arrive(&ctl.ready[g]);
+      ++it;
       have = more;
     }
     if (!ok && lane == 0) raise_abort(ctl, a.err);

@@ -306,6 +306,34 @@ __device__ __forceinline__ void mma_ts_tile_chunk_elect(uint32_t d, uint32_t a, 
       : "memory");
 }
 
+// Both K-chunks of a pair for one A tile: 8 MMAs behind one elect.sync, chunk 0
+// from A columns a0 / B descriptor b0, chunk 1 from a1 / b1 (4 K-steps of 16
+// each: A + 8 columns, B + 32 bytes). Only the first MMA takes `accumulate`.
+__device__ __forceinline__ void mma_ts_tile_pair_elect(uint32_t d, uint32_t a0, uint32_t a1,
+                                                       uint64_t b0, uint64_t b1, uint32_t idesc,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      ".reg .b32 x1, x2, x3, y1, y2, y3;\n\t"
+      ".reg .b64 u1, u2, u3, v1, v2, v3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"
+      "add.u32 y1, %2, 8;\n\tadd.u32 y2, %2, 16;\n\tadd.u32 y3, %2, 24;\n\t"
+      "add.u64 u1, %3, 2;\n\tadd.u64 u2, %3, 4;\n\tadd.u64 u3, %3, 6;\n\t"
+      "add.u64 v1, %4, 2;\n\tadd.u64 v2, %4, 4;\n\tadd.u64 v3, %4, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], u1, %5, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], u2, %5, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], u3, %5, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %5, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [y1], v1, %5, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [y2], v2, %5, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [y3], v3, %5, 1;\n\t}" ::"r"(d),
+      "r"(a0), "r"(a1), "l"(b0), "l"(b1), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // mma_commit issued by one elected lane of a converged warp.
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
