@@ -53,7 +53,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="t4096")
-    p.add_argument("--block-m", type=int, default=128)
+    p.add_argument("--block-m", default="auto",
+                   help="tile rows of the block map; auto = 64 for short expert groups, else 128")
     p.add_argument("--sets", type=int, default=2, help="independent layer sets cycled per step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -411,6 +412,13 @@ def run_ours(args):
 
 def main():
     args = parse_args()
+    from routing_q4_grouped_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]
+    if args.block_m == "auto":
+        # same rule as moeq4.default_block_m (no library load needed for the reference arm)
+        args.block_m = 64 if cfg.tokens_per_call * cfg.k <= 32 * cfg.E else 128
+    else:
+        args.block_m = int(args.block_m)
     if args.impl == "reference":
         run_reference(args)
     else:

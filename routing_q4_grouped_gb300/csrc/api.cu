@@ -205,8 +205,9 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
   uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
   uint16_t* act_sh = reinterpret_cast<uint16_t*>(base + L.act_sh);
   const uint64_t act_rows = act_rows_capacity(T, k, max_tiles);
-  const uint64_t act_sh_rows = (static_cast<uint64_t>(T) + gemm_tile_rows() - 1) /
-                               gemm_tile_rows() * gemm_tile_rows();
+  const int tile_rows = gemm_tile_rows(r->block_m);
+  // the shared activation rows are allocated up to a multiple of 128 (either tile height)
+  const uint64_t act_sh_rows = (static_cast<uint64_t>(T) + 127) / 128 * 128;
   GemmArgs a{};
   a.E = E;
   a.T = T;
@@ -222,7 +223,7 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
   a.y_acc = reinterpret_cast<float*>(base + L.y_acc);
   a.err = r->err;
   a.timeout_ns = timeout_ns();
-  const int n_sh_tiles = fs ? (T + gemm_tile_rows() - 1) / gemm_tile_rows() : 0;
+  const int n_sh_tiles = fs ? (T + tile_rows - 1) / tile_rows : 0;
 
   const CUtensorMapSwizzle SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -244,7 +245,7 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
     else m.C_sh = m.C;
     m.B_sh = m.B;
     if (!ok) return MOE_ERR_CUDA;
-    if (launch_gemm(0, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(0, tile_rows, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
     stage_mark(3, s);
   }
   // ---- pass 1: down + weighted combine (+ shared expert)
@@ -264,7 +265,7 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
     m.C = m.B;
     m.C_sh = m.B_sh;
     if (!ok) return MOE_ERR_CUDA;
-    if (launch_gemm(1, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(1, tile_rows, g, m, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
     stage_mark(4, s);
   }
   if (launch_finalize(a.y_acc, y, static_cast<size_t>(T) * d, s) != cudaSuccess)

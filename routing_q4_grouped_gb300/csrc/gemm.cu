@@ -36,10 +36,12 @@
 //                issues every pair's 8 MMAs of A tile j into accumulator j; the
 //                two run in parallel, each as a whole warp with warp-uniform
 //                operands and one elected lane issuing
-// Tensor memory: columns [0, 256) hold 4 chunk stages of 64 columns (tile j at
-// +32 j; stages 2s and 2s+1 form pair stage s), [256, 512) the two
-// accumulators (A tile j -> 256 + 128 j), each released as soon as the
-// epilogue has read it.
+// Tensor memory: pair stages of 128 columns (chunk h at +64 h, tile j at +32 j)
+// followed by the two accumulators, each released as soon as the epilogue has
+// read it. Units of up to 128 token rows: 2 pair stages in [0, 256),
+// accumulators at 256 + 128 j. Units of up to 64 rows (a block map of 64-row
+// tiles, for short expert groups): 3 pair stages in [0, 384), accumulators at
+// 384 + 64 j.
 //
 // Pass 0 (gate/up): A tile j covers 64 output features with gate and up rows
 //   interleaved in blocks of 8 (TMEM lanes 16m..16m+7 = gate rows of features
@@ -67,13 +69,11 @@ namespace moeq4 {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kNMax = 128;                 // rows per unit (MMA N)
-constexpr int kStages = 4;                 // chunk stages of dequantised weights in TMEM
-constexpr int kPairStages = kStages / 2;   // a K-pair of chunk stages per barrier
-constexpr int kBSlotsMax = 4;              // pair slots of token rows in shared memory (pass 0)
+constexpr int kNMax = 128;                 // largest rows per unit (MMA N)
+constexpr int kPairStagesMax = 3;
+constexpr int kBSlotsMax = 4;              // pair slots of token rows in shared memory
 constexpr int kACols = 64;                 // TMEM columns per chunk stage (2 tiles x 32)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = 256;            // accumulator of tile j at column 256 + 128 j
 constexpr int kDqWarps = 16;               // warp w: pairs of parity w/8, A tile (w/4)%2
 constexpr int kDqGroupWarps = 8;           // warps per pair-parity group
 constexpr int kEpiWarp0 = 16;              // warp % 4 = TMEM lane quarter
@@ -84,16 +84,31 @@ constexpr int kMmaWarp0 = 26;              // two MMA issuers: warp 26 + A tile
 constexpr int kThreads = 28 * 32;
 static_assert(kThreads == kGemmThreads, "thread count");
 
-constexpr int kBBytes = kNMax * 128;       // token rows of one K-chunk: 64 bf16 (128 B) each, 128B swizzle
-constexpr int kSlotBytes = 2 * kBBytes;    // a pair of K-chunks
 constexpr size_t kOffB = 0;
 constexpr int kStageRow = 256;             // pass 1 staging: fp32 outputs of a unit per token row
+
+// Geometry for units of at most NMAX (128 or 64) token rows. Tensor memory holds
+// the dequantised A pair stages (128 columns each: chunk h at +64 h, tile j at
+// +32 j) followed by the two accumulators (tile j at kDCol + NMAX j). With
+// NMAX = 64 the accumulators take half the columns, which buys a third pair
+// stage: more slack between the dequant groups and the MMAs when units are
+// short and the weights stream from HBM.
+template <int NMAX>
+struct Geo {
+  static_assert(NMAX == 64 || NMAX == 128, "unit rows");
+  static constexpr int kPairStages = NMAX == 64 ? 3 : 2;
+  static constexpr uint32_t kDCol = kPairStages * 2 * kACols;
+  static constexpr int kBBytes = NMAX * 128;  // token rows of one K-chunk: 64 bf16 (128 B) each, 128B swizzle
+  static constexpr int kSlotBytes = 2 * kBBytes;   // a pair of K-chunks
+  static_assert(kDCol + 2 * NMAX <= kTmemCols, "tensor memory columns");
+  static_assert(kPairStages <= kPairStagesMax, "pair stages");
+};
 
 struct Ctl {
   uint64_t b_full[kBSlotsMax];   // token-row slot landed (transaction bytes)
   uint64_t b_empty[kBSlotsMax];  // token-row slot's MMAs retired (both MMA warps)
-  uint64_t ready[kPairStages];    // pair stage written by its dequant group
-  uint64_t consumed[kPairStages]; // pair stage's MMAs retired (both MMA warps)
+  uint64_t ready[kPairStagesMax];    // pair stage written by a dequant group
+  uint64_t consumed[kPairStagesMax]; // pair stage's MMAs retired (both MMA warps)
   uint64_t d_full;            // both MMA warps committed the unit
   uint64_t drain2;
   uint64_t d_empty[2];
@@ -107,19 +122,21 @@ struct Ctl {
 };
 
 // Shared memory of each pass. Pass 0: four token-row pair slots and two bf16
-// activation tiles for the TMA stores. Pass 1: two token-row pair slots (tile
-// loads of L2-resident activations need less lookahead than gathers) and a
-// [128 tokens][256 features] fp32 staging area that takes a unit's outputs out
-// of tensor memory, so the accumulators are released before the reductions run.
-template <int MODE>
+// activation tiles for the TMA stores. Pass 1: token-row pair slots (two for
+// 128-row units: tile loads of L2-resident activations need less lookahead
+// than gathers) and a [NMAX tokens][256 features] fp32 staging area that takes
+// a unit's outputs out of tensor memory, so the accumulators are released
+// before the reductions run.
+template <int MODE, int NMAX>
 struct Layout {
-  static constexpr int kBSlots = MODE == 0 ? 4 : 2;
-  static constexpr size_t kEpi = MODE == 0 ? 32768 : size_t(kNMax) * kStageRow * 4;
-  static constexpr size_t kOffEpi = kOffB + size_t(kBSlots) * kSlotBytes;
+  static constexpr int kBSlots = (MODE == 0 || NMAX == 64) ? 4 : 2;
+  static constexpr size_t kEpi = MODE == 0 ? 32768 : size_t(NMAX) * kStageRow * 4;
+  static constexpr size_t kOffEpi = kOffB + size_t(kBSlots) * Geo<NMAX>::kSlotBytes;
   static constexpr size_t kOffCtl = kOffEpi + kEpi;
   static constexpr size_t kSmem = 1024 + kOffCtl + sizeof(Ctl);
+  static_assert(kBSlots <= kBSlotsMax, "token-row slots");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
-static_assert(Layout<1>::kSmem <= 227 * 1024 && Layout<0>::kSmem <= 227 * 1024, "shared memory");
 
 struct Unit {
   int e, row0, rows, p, K;
@@ -127,7 +144,9 @@ struct Unit {
   bool shared;
 };
 
-// Unit u -> (tile, unit column p). Routed units first, tile-major, then shared.
+// Unit u -> (tile, unit column p). Routed units first, tile-major, then shared
+// (shared tiles of NMAX rows).
+template <int NMAX>
 __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, Unit& U) {
   const int n_routed = n_rt * a.n_fb;
   if (u < n_routed) {
@@ -140,7 +159,7 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
     U.shared = false;
     U.K = a.K;
     U.act0 = act_tile_base(U.row0, ti);
-    if (U.e < 0 || U.e >= a.E || U.rows < 1 || U.rows > kNMax || U.row0 < 0 ||
+    if (U.e < 0 || U.e >= a.E || U.rows < 1 || U.rows > NMAX || U.row0 < 0 ||
         static_cast<long long>(U.row0) + U.rows > static_cast<long long>(a.T) * a.k)
       return false;
   } else {
@@ -148,8 +167,8 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
     const int st = v / a.n_fb_sh;
     U.p = v - st * a.n_fb_sh;
     U.e = 0;
-    U.row0 = st * kNMax;
-    U.rows = min(kNMax, a.T - U.row0);
+    U.row0 = st * NMAX;
+    U.rows = min(NMAX, a.T - U.row0);
     U.shared = true;
     U.K = a.K_sh;
     U.act0 = U.row0;
@@ -189,12 +208,13 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 
 // Next (unit, pair) of this CTA's sequence; u starts at blockIdx.x - gridDim.x
 // with pi == npair == 0. Returns false when the sequence is exhausted.
+template <int NMAX>
 __device__ __forceinline__ bool next_pair(const GemmArgs& a, int n_rt, int total, int& u, int& pi,
                                           int& npair, const uint8_t*& blocks) {
   if (++pi < npair) return true;
   for (u += gridDim.x; u < total; u += gridDim.x) {
     Unit U;
-    if (decode_unit(a, n_rt, u, U)) {
+    if (decode_unit<NMAX>(a, n_rt, u, U)) {
       pi = 0;
       npair = U.K / 128;
       blocks = unit_blocks(a, U);
@@ -240,7 +260,7 @@ __device__ __forceinline__ void dequant_chunk(const ChunkWords& w, uint32_t (&v)
   dequant8(w.hi.w, s2, b2, v + 28);
 }
 
-template <int MODE>
+template <int MODE, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     q4_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB_sh,
@@ -249,10 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  using G = Geo<NMAX>;
+  using Lay = Layout<MODE, NMAX>;
+  constexpr int kBSlots = Lay::kBSlots;
+  constexpr int kPairStages = G::kPairStages;
+  constexpr int kBBytes = G::kBBytes;
+  constexpr int kSlotBytes = G::kSlotBytes;
+  constexpr uint32_t kDCol = G::kDCol;
   uint8_t* sB = smem + kOffB;
-  constexpr int kBSlots = Layout<MODE>::kBSlots;
-  uint8_t* sEpi = smem + Layout<MODE>::kOffEpi;
-  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + Layout<MODE>::kOffCtl);
+  uint8_t* sEpi = smem + Lay::kOffEpi;
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + Lay::kOffCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -305,20 +331,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_x = policy_evict_last();   // token rows: reused by every unit of a tile
     if (lead && static_cast<int>(blockIdx.x) < total) {
       Unit U0;
-      if (decode_unit(a, n_rt, blockIdx.x, U0)) prefetch_unit(a, U0);
+      if (decode_unit<NMAX>(a, n_rt, blockIdx.x, U0)) prefetch_unit(a, U0);
     }
     uint32_t ip = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
-      if (!decode_unit(a, n_rt, u, U)) {
+      if (!decode_unit<NMAX>(a, n_rt, u, U)) {
         if (lead) atomicOr(a.err, MOE_DEVERR_BAD_TILE);
         continue;
       }
       if (lead) {   // the next unit's weights head for L2 while this one runs
         const int v = u + gridDim.x;
         Unit V;
-        if (v < total && decode_unit(a, n_rt, v, V)) prefetch_unit(a, V);
+        if (v < total && decode_unit<NMAX>(a, n_rt, v, V)) prefetch_unit(a, V);
       }
       const int npad = (U.rows + 15) & ~15;
       const CUtensorMap* mB = U.shared ? &tmB_sh : &tmB;
@@ -381,10 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ip = 0, nu = 0;
     bool ok = true;
     const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
-    const uint32_t dcol = tmem + kDCol + 128 * j;
+    const uint32_t dcol = tmem + kDCol + NMAX * j;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       Unit U;
-      if (!decode_unit(a, n_rt, u, U)) continue;
+      if (!decode_unit<NMAX>(a, n_rt, u, U)) continue;
       const uint32_t npad = (U.rows + 15) & ~15;
       const uint32_t idesc = idesc_bf16_f32(128, npad);
       const int npair = U.K / 128;
@@ -415,9 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kDqWarps) {
     // ------------------------------------------------------ dequantisation
     // Two groups of eight warps take turns: group g = w/8 expands the pairs of
-    // the CTA's sequence whose index has parity g, always into pair stage g;
-    // warp w covers A tile (w/4)%2, TMEM lane quarter w%4, both chunks of the
-    // pair. Each group's ready barrier completes once its eight warps have
+    // the CTA's sequence whose index ip has parity g, into pair stage
+    // ip % kPairStages (with two stages: always stage g); warp w covers A tile
+    // (w/4)%2, TMEM lane quarter w%4, both chunks of the pair. A stage's ready
+    // barrier completes once the eight warps of the group that wrote it have
     // stored the pair. The groups run a pair apart, so one group's stores
     // overlap the other's arithmetic, and a warp's loads of its next pair are
     // issued as soon as the registers free, two pairs of the sequence ahead.
@@ -425,44 +452,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = (warp >> 2) & 1;    // A tile
     const int g = warp >> 3;          // pair parity
     const int L = q * 32 + lane;      // TMEM lane = A row
-    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j + 2 * g * kACols;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + 32 * j;
     const uint32_t roff = j * 4096 + L * 16;          // row codes (chunk h: + h * kPackChunkBytes)
     const uint32_t soff = 8192 + (j * 128 + L) * 4;   // scale|bias
     int cu = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), cpi = 0, cnp = 0;
     const uint8_t* cbl = nullptr;
     ChunkWords n0, n1;
-    bool have = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
-    if (have && g == 1) have = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+    bool have = next_pair<NMAX>(a, n_rt, total, cu, cpi, cnp, cbl);
+    if (have && g == 1) have = next_pair<NMAX>(a, n_rt, total, cu, cpi, cnp, cbl);
     if (have) {
       const uint8_t* pb = cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes);
       load_chunk(pb, roff, soff, n0);
       load_chunk(pb + kPackChunkBytes, roff, soff, n1);
     }
-    uint32_t it = 0;
+    uint32_t ip = g;                  // index of the pair in the CTA's sequence
     bool ok = true;
     while (have) {
-      bool more = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
-      if (more) more = next_pair(a, n_rt, total, cu, cpi, cnp, cbl);
+      bool more = next_pair<NMAX>(a, n_rt, total, cu, cpi, cnp, cbl);
+      if (more) more = next_pair<NMAX>(a, n_rt, total, cu, cpi, cnp, cbl);
       const uint8_t* pb = more ? cbl + static_cast<size_t>(cpi) * (2 * kPackChunkBytes) : nullptr;
-      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[g], (it & 1u) ^ 1u, abortp, lim))) {
+      const uint32_t ps = ip % kPairStages;
+      if (!__all_sync(kFull, mbar_wait(&ctl.consumed[ps], ((ip / kPairStages) & 1u) ^ 1u, abortp,
+                                       lim))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t t = tq + ps * (2 * kACols);
       uint32_t v[32];
       dequant_chunk(n0, v);
       if (more) load_chunk(pb, roff, soff, n0);
-      tmem_st_32x32b_x16(tq, *reinterpret_cast<const uint32_t(*)[16]>(v));
-      tmem_st_32x32b_x16(tq + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
+      tmem_st_32x32b_x16(t, *reinterpret_cast<const uint32_t(*)[16]>(v));
+      tmem_st_32x32b_x16(t + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
       dequant_chunk(n1, v);
       if (more) load_chunk(pb + kPackChunkBytes, roff, soff, n1);
-      tmem_st_32x32b_x16(tq + kACols, *reinterpret_cast<const uint32_t(*)[16]>(v));
-      tmem_st_32x32b_x16(tq + kACols + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
+      tmem_st_32x32b_x16(t + kACols, *reinterpret_cast<const uint32_t(*)[16]>(v));
+      tmem_st_32x32b_x16(t + kACols + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.ready[g]);
-      ++it;
+      if (lane == 0) mbar_arrive(&ctl.ready[ps]);
+      ip += 2;
       have = more;
     }
     if (!ok && lane == 0) raise_abort(ctl, a.err);
@@ -499,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prefetch_rows = [&](int from, int& tt, float& wv) {
       for (int v = from; v < total; v += gridDim.x) {
         Unit V;
-        if (decode_unit(a, n_rt, v, V)) {
+        if (decode_unit<NMAX>(a, n_rt, v, V)) {
           row_info(V, tt, wv);
           return;
         }
@@ -511,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nu = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       Unit U;
-      if (!decode_unit(a, n_rt, u, U)) continue;
+      if (!decode_unit<NMAX>(a, n_rt, u, U)) continue;
       const int npad = (U.rows + 15) & ~15;
       const uint32_t db = nu & 1u;
       if (MODE == 1) {
@@ -565,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_16x256b_x4(taddr_q + kDCol, ra);
         for (int jt = 0; jt < 2; ++jt) {
           for (int cc = 0; cc < ncc; ++cc) {
-            const uint32_t col = taddr_q + kDCol + 128 * jt + 32 * cc;
+            const uint32_t col = taddr_q + kDCol + NMAX * jt + 32 * cc;
             uint8_t* srow = sEpi + jt * 16384 + tc * 128 + cc * 32 * 128;
             tmem_ld_wait();
             tmem_regs_ready(ra);
@@ -577,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!last)
               tmem_ld_16x256b_x4(col + 32, ra);
             else if (jt == 0)
-              tmem_ld_16x256b_x4(taddr_q + kDCol + 128, ra);
+              tmem_ld_16x256b_x4(taddr_q + kDCol + NMAX, ra);
             put(rb, srow, 1);
           }
           tc_fence_before();                                // accumulator jt fully read
@@ -608,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* col = stg + 128 * jt + 32 * q + lane;       // this thread's feature column
           for (int cc = 0; cc * 32 < npad; ++cc) {
             uint32_t dv[32];
-            tmem_ld_32x32b_x32(taddr_q + kDCol + 128 * jt + cc * 32, dv);
+            tmem_ld_32x32b_x32(taddr_q + kDCol + NMAX * jt + cc * 32, dv);
             tmem_ld_wait();   // only stores (ordered by the wait's memory clobber) follow
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) col[(cc * 32 + jj) * kStageRow] = __uint_as_float(dv[jj]);
@@ -667,18 +697,19 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
   }
 }
 
-template <int MODE>
+template <int MODE, int NMAX>
 cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s) {
+  using Lay = Layout<MODE, NMAX>;
   static bool attr_set = false;   // per process; the attribute is per function
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(q4_grouped_gemm_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(q4_grouped_gemm_kernel<MODE, NMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Layout<MODE>::kSmem));
+                                         static_cast<int>(Lay::kSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  q4_grouped_gemm_kernel<MODE><<<grid, kThreads, Layout<MODE>::kSmem, s>>>(m.B, m.B_sh, m.C, m.C_sh,
-                                                                         a);
+  q4_grouped_gemm_kernel<MODE, NMAX><<<grid, kThreads, Lay::kSmem, s>>>(m.B, m.B_sh, m.C, m.C_sh,
+                                                                      a);
   return cudaGetLastError();
 }
 
@@ -703,13 +734,18 @@ FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles) {
   return w;
 }
 
-int gemm_tile_rows() { return kNMax; }
+int gemm_tile_rows(int block_m) { return block_m <= 64 ? 64 : kNMax; }
 
-size_t gemm_smem_bytes() { return std::max(Layout<0>::kSmem, Layout<1>::kSmem); }
+size_t gemm_smem_bytes() {
+  return std::max({Layout<0, 128>::kSmem, Layout<1, 128>::kSmem, Layout<0, 64>::kSmem,
+                   Layout<1, 64>::kSmem});
+}
 
-cudaError_t launch_gemm(int mode, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s) {
-  if (mode == 0) return launch_mode<0>(a, m, grid, s);
-  return launch_mode<1>(a, m, grid, s);
+cudaError_t launch_gemm(int mode, int tile_rows, const GemmArgs& a, const GemmMaps& m, int grid,
+                        cudaStream_t s) {
+  if (tile_rows == 64) return mode == 0 ? launch_mode<0, 64>(a, m, grid, s) : launch_mode<1, 64>(a, m, grid, s);
+  if (tile_rows != kNMax) return cudaErrorInvalidValue;
+  return mode == 0 ? launch_mode<0, 128>(a, m, grid, s) : launch_mode<1, 128>(a, m, grid, s);
 }
 
 cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStream_t s) {

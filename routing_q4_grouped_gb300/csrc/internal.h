@@ -107,7 +107,7 @@ struct GemmArgs {
   const float* wts;         // [T*k] routing weights
   int n_fb;                 // units (256 weight rows) per routed tile
   int n_fb_sh;              // units per shared tile
-  int n_sh_tiles;           // shared tiles (gemm_tile_rows() rows each)
+  int n_sh_tiles;           // shared tiles (gemm_tile_rows(block_m) rows each)
   const uint8_t* pk;        // packed routed matrix of this pass
   const uint8_t* pk_sh;     // packed shared-expert matrix of this pass
   float* y_acc;             // [T][d] fp32 combine buffer (zeroed by pass 0)
@@ -133,12 +133,17 @@ struct FfnWs {
 };
 FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles);
 
-// mode 0: gate/up + SwiGLU -> act (also zeroes y_acc); mode 1: down + weighted combine -> y_acc
-cudaError_t launch_gemm(int mode, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s);
+// mode 0: gate/up + SwiGLU -> act (also zeroes y_acc); mode 1: down + weighted combine -> y_acc.
+// tile_rows = gemm_tile_rows(block_m) of the block map the units come from.
+cudaError_t launch_gemm(int mode, int tile_rows, const GemmArgs& a, const GemmMaps& m, int grid,
+                        cudaStream_t s);
 
 cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStream_t s);
 
 size_t gemm_smem_bytes();
-int gemm_tile_rows();   // max rows per unit and rows per shared-expert tile (128)
+// Max rows per unit and rows per shared-expert tile for a block map of at most
+// block_m rows per tile: 64 when block_m <= 64 (deeper tensor-memory pipeline),
+// else 128.
+int gemm_tile_rows(int block_m);
 
 }  // namespace moeq4

@@ -315,10 +315,21 @@ def moe_debug_set_stage_events(events) -> None:
     _check("moe_debug_set_stage_events", lib().moe_debug_set_stage_events(arr, len(events)))
 
 
-class Layer:
-    """Convenience owner of the buffers one layer call needs (T tokens)."""
+def default_block_m(T: int, E: int, k: int) -> int:
+    """Tile height of the block map for a batch of T tokens: 64 when the expert
+    groups average at most 32 rows (short groups, weights streamed from HBM:
+    the 64-row kernels keep a deeper tensor-memory pipeline), else 128 (every
+    weight tile expanded once per 128 token rows)."""
+    return 64 if T * k <= 32 * E else 128
 
-    def __init__(self, W: DeviceWeights, T: int, k: int, block_m: int = 128, device="cuda"):
+
+class Layer:
+    """Convenience owner of the buffers one layer call needs (T tokens);
+    block_m=None picks default_block_m(T, E, k)."""
+
+    def __init__(self, W: DeviceWeights, T: int, k: int, block_m=128, device="cuda"):
+        if block_m is None:
+            block_m = default_block_m(T, W.E, k)
         self.W, self.T, self.k = W, T, k
         self.route = RouteBuffers.alloc(T, W.E, k, block_m, device)
         self.ws = alloc_workspace(moe_layer_workspace_size(T, W.E, k, W.d, W.f, W.f_s, block_m), device)

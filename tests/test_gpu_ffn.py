@@ -57,6 +57,17 @@ def test_t512_full():
     _run(synth.CONFIGS["t512"])
 
 
+def test_t512_full_64_row_tiles():
+    # block map of 64-row tiles: the kernels with three tensor-memory pair stages
+    _run(synth.CONFIGS["t512"], block_m=64)
+
+
+@pytest.mark.parametrize("T", [45, 129])
+def test_tiny_ragged_with_shared_64_row_tiles(T):
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], f_s=128)
+    _run(cfg, T=T, block_m=64)
+
+
 def test_t4096_sampled():
     cfg = synth.CONFIGS["t4096"]
     rng = np.random.default_rng(11)
@@ -67,6 +78,13 @@ def test_skew_sampled():
     cfg = synth.CONFIGS["skew"]
     rng = np.random.default_rng(12)
     _run(cfg, sample=np.concatenate([[0, cfg.T - 1], rng.integers(0, cfg.T, 62)]))
+
+
+def test_skew_sampled_64_row_tiles():
+    # large groups split into many 64-row tiles, empty experts, ragged tails
+    cfg = synth.CONFIGS["skew"]
+    rng = np.random.default_rng(14)
+    _run(cfg, block_m=64, sample=np.concatenate([[0, cfg.T - 1], rng.integers(0, cfg.T, 62)]))
 
 
 def test_single_expert_all_rows():
