@@ -41,8 +41,10 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer prefill tokens/s at T=4096; grouped-GEMM % of GB300 BF16 TC peak"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-STAGES = ["route_select_scan", "route_scatter", "gemm_gate_up_swiglu", "gemm_down_combine",
-          "finalize_bf16"]
+# stage events 0..5 bracket: routing (one kernel; events 1 and 2 coincide), gate/up
+# GEMM, down GEMM, bf16 finalize
+STAGES = ["route", None, "gemm_gate_up_swiglu", "gemm_down_combine", "finalize_bf16"]
+LAUNCHES_PER_LAYER = 4
 KERNEL_SOURCES = ["gemm.cu", "dequant.cuh", "ptx.cuh"]
 
 
@@ -300,10 +302,10 @@ def run_ours(args):
     ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
     ms_step = ms_total / args.steps
     value = T * world * args.steps / (ms_total * 1e-3)
-    launches = 5 * args.steps
+    launches = LAUNCHES_PER_LAYER * args.steps
 
     # ---- per-kernel times over the same K steps, stage events on the launching stream
-    stage_ms = {s: [] for s in STAGES}
+    stage_ms = {s: [] for s in STAGES if s}
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     for row in evs:             # torch creates the CUDA event on first record
         for e in row:
@@ -316,7 +318,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     for i in range(args.steps):
         for j, s in enumerate(STAGES):
-            stage_ms[s].append(evs[i][j].elapsed_time(evs[i][j + 1]))
+            if s:
+                stage_ms[s].append(evs[i][j].elapsed_time(evs[i][j + 1]))
     kern = {s: statistics.mean(v) for s, v in stage_ms.items()}
 
     # ---- end to end through the public call: pinned H2D of x + logits, layer, D2H of y

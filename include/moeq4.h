@@ -159,7 +159,10 @@ size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int3
  *   out     result arrays and T, E, k, block_m (host struct, device arrays)
  *   ws      scratch of moe_route_workspace_size(T, E, k) bytes
  * T = 0 is allowed (counts/offsets zeroed, n_tiles = 0; logits, ids, w, perm
- * and inv may then be NULL). */
+ * and inv may then be NULL). The step is one cooperative kernel launch (its
+ * blocks meet at a grid barrier, so the device must hold all of them at once;
+ * the block size grows with T to keep the grid resident); a launch the device
+ * refuses returns MOE_ERR_CUDA. */
 moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, size_t ws_bytes,
                      void* stream);
 
@@ -168,7 +171,7 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  * such as a serving process that reserves all device memory up front and hands
  * out fixed arenas, or a plugin that has no access to its host framework's
  * allocator. Same inputs, outputs and results as moe_route, but its scratch is
- * a fixed array inside the library (about 770 KB, held on every GPU that loads
+ * a fixed array inside the library (about 1 MB, held on every GPU that loads
  * the library until the process exits), so:
  *  - sizes are limited to T <= 8192, E <= 256, k <= 8; larger ones return
  *    MOE_ERR_TOO_LARGE and enqueue nothing;

@@ -146,7 +146,6 @@ RouteArgs make_route_args(const float* logits, const moe_route_out* r, void* ws)
   a.E = r->E;
   a.k = r->k;
   a.block_m = r->block_m;
-  a.nblk = r->T > 0 ? (r->T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock : 1;
   a.ids = r->ids;
   a.w = r->w;
   a.counts = r->counts;
@@ -156,9 +155,7 @@ RouteArgs make_route_args(const float* logits, const moe_route_out* r, void* ws)
   a.tiles = r->tiles;
   a.n_tiles = r->n_tiles;
   a.err = r->err;
-  a.lb = reinterpret_cast<uint32_t*>(base + L.lb);
-  a.blk_base = reinterpret_cast<int32_t*>(base + L.blk_base);
-  a.lrank = reinterpret_cast<int32_t*>(base + L.lrank);
+  a.lb = reinterpret_cast<uint64_t*>(base + L.lb);
   a.ctr = reinterpret_cast<int32_t*>(base + L.ctr);
   a.timeout_ns = timeout_ns();
   return a;
@@ -175,10 +172,9 @@ moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, siz
   if ((st = device_info(&di)) != MOE_OK) return st;
   const RouteArgs a = make_route_args(logits, r, ws);
   stage_mark(0, s);
-  if (launch_route_select(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(a, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
   stage_mark(1, s);
-  if (launch_route_scatter(a, s) != cudaSuccess) return MOE_ERR_CUDA;
-  stage_mark(2, s);
+  stage_mark(2, s);   // (one routing kernel: stages 1 and 2 coincide)
   return MOE_OK;
 }
 
@@ -280,9 +276,9 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 constexpr int kNoAllocMaxT = 8192;
 constexpr int kNoAllocMaxE = 256;
 constexpr int kNoAllocMaxK = 8;
-// routing scratch at the limits: lookback words and block bases of 256 blocks x 256
-// experts, 2 counters, local ranks of 65536 rows (each area 256-byte aligned)
-constexpr size_t kNoAllocBytes = 262144 + 256 + 262144 + 262144;
+// routing scratch at the limits: counters (256 bytes) and the 8-byte lookback
+// words of 1024 blocks (8192 tokens in blocks of at least 8) x 256 experts
+constexpr size_t kNoAllocBytes = 256 + 8 * 1024 * 256;
 __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
 // Device address of g_route_scratch on the current device, looked up once per
@@ -435,8 +431,9 @@ moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the lookback words and counters must start at zero (each call also leaves them zero)
-  if (cudaMemsetAsync(ws, 0, L.blk_base, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the ticket and leave counters must start at zero (each call also leaves them
+  // zero); the epoch counter and the lookback words may hold anything
+  if (cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   return route_impl(logits, out, ws, kNoAllocBytes, s);
 }
 

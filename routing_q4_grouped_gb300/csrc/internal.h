@@ -11,18 +11,21 @@ namespace moeq4 {
 
 // ----------------------------------------------------------------- routing
 
-constexpr int kRouteTokensPerBlock = 32;   // tokens per selection block (8 warps x 4)
-constexpr int kRouteThreads = 256;
-
-// Lookback word: 2-bit status | 30-bit count.
-constexpr uint32_t kLbAggregate = 1u << 30;
-constexpr uint32_t kLbInclusive = 2u << 30;
-constexpr uint32_t kLbValueMask = (1u << 30) - 1;
+constexpr int kRouteThreads = 256;         // threads per routing block (8 warps)
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteTokensMin = 8;         // tokens per block at least (2 warps select when k <= 8)
+constexpr int kRouteBlocksTarget = 128;    // blocks per call aimed at (longer lookback chains
+                                           // beyond), fewer tokens per block when T is small
+// Routing counters at the start of the workspace.
+constexpr int kCtrTicket = 0;              // block arrival order = block id (zero between calls)
+constexpr int kCtrLeave = 1;               // blocks done (zero between calls)
+constexpr int kCtrEpoch = 2;               // call number: tags this call's lookback words
 
 struct RouteArgs {
   const float* logits;
   int T, E, k, block_m;
-  int nblk;                 // selection blocks = max(1, ceil(T / kRouteTokensPerBlock))
+  int tpb;                  // tokens per block (set at launch)
+  int nblk;                 // blocks = max(1, ceil(T / tpb)) (set at launch)
   int32_t* ids;
   float* w;
   int32_t* counts;
@@ -33,20 +36,23 @@ struct RouteArgs {
   int32_t* n_tiles;
   int32_t* err;
   // scratch
-  uint32_t* lb;             // [nblk][E] lookback words (zero between calls)
-  int32_t* blk_base;        // [nblk][E] exclusive prefix of earlier blocks' counts
-  int32_t* lrank;           // [T*k] rank of (t, j) among its block's rows of the same expert
-  int32_t* ctr;             // [2] ticket, done (zero between calls)
+  uint64_t* lb;             // [nblk][E] lookback words (epoch | status | count)
+  int32_t* ctr;             // [3] counters
   uint64_t timeout_ns;
 };
 
+// Most blocks a call over T tokens can use (blocks of at least kRouteTokensMin tokens).
+inline int route_max_blocks(int T) {
+  return T > 0 ? (T + kRouteTokensMin - 1) / kRouteTokensMin : 1;
+}
+
 struct RouteWs {
-  size_t lb, blk_base, lrank, ctr, total;
+  size_t ctr, lb, total;
 };
 RouteWs route_ws_layout(int T, int E, int k);
 
-cudaError_t launch_route_select(const RouteArgs& a, cudaStream_t s);   // kernel 1
-cudaError_t launch_route_scatter(const RouteArgs& a, cudaStream_t s);  // kernel 2
+// The whole routing step: one cooperative launch (sms = multiprocessors).
+cudaError_t launch_route(const RouteArgs& a, int sms, cudaStream_t s);
 
 // Optional stage events (bench/test timing): mark(i) records event i on `s`.
 void stage_mark(int i, cudaStream_t s);

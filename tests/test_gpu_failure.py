@@ -1,12 +1,13 @@
 """Failure detection on the GPU without a fault, trap or hang.
 
-A routing call whose scratch counters were left dirty makes half of the
-selection blocks refuse their (out-of-range) block ids and leaves the others'
-decoupled-lookback waits without predecessors: those waits run out after the
-configured limit, every kernel returns, and the error word carries both
-MOE_DEVERR_BAD_WORKSPACE and MOE_DEVERR_SCAN_TIMEOUT. The scatter kernel's own
-checks keep every write inside its buffer. The wait limit is read once per
-process, so the call runs in a child process with MOEQ4_WAIT_TIMEOUT_MS=100.
+A routing call whose block-ticket counter was left dirty (1 instead of 0)
+hands out ids 1..nblk: the block that draws nblk refuses it (out of range), so
+the grid barrier never fills, and no block has id 0, so the decoupled-lookback
+waits never find an inclusive prefix. Both waits run out after the configured
+limit, the kernel returns, and the error word carries MOE_DEVERR_BAD_WORKSPACE
+and MOE_DEVERR_SCAN_TIMEOUT; the scatter's own checks keep every write inside
+its buffer. The wait limit is read once per process, so the call runs in a
+child process with MOEQ4_WAIT_TIMEOUT_MS=100.
 """
 import os
 import subprocess
@@ -27,9 +28,7 @@ lg = torch.from_numpy(synth.gen_logits(cfg)).cuda()
 T, E = lg.shape
 out = moeq4.RouteBuffers.alloc(T, E, cfg.k, 128)
 ws = moeq4.alloc_workspace(moeq4.moe_route_workspace_size(T, E, cfg.k))
-nblk = (T + 31) // 32
-ctr = (4 * nblk * E + 255) // 256 * 256          # the counters follow the lookback words
-ws[ctr:ctr + 4].view(torch.int32)[0] = nblk // 2  # ticket counter left dirty
+ws[0:4].view(torch.int32)[0] = 1                 # the ticket counter opens the workspace
 torch.cuda.synchronize()
 t0 = time.time()
 moeq4.moe_route(lg, out, ws)
