@@ -79,7 +79,8 @@ constexpr int kDqGroupWarps = 8;           // warps per pair-parity group
 constexpr int kEpiWarp0 = 16;              // warp % 4 = TMEM lane quarter
 constexpr int kEpiWarps = 4;
 constexpr int kProdWarp0 = 20;
-constexpr int kProdWarps = 6;
+constexpr int kProdWarps = 6;              // warps 20-25 (pass 0: all producers)
+constexpr int kProdWarpsDown = 2;          // pass 1: warps 20-21 produce, 22-25 add rows
 constexpr int kMmaWarp0 = 26;              // two MMA issuers: warp 26 + A tile
 constexpr int kThreads = 28 * 32;
 static_assert(kThreads == kGemmThreads, "thread count");
@@ -260,6 +261,23 @@ __device__ __forceinline__ void dequant_chunk(const ChunkWords& w, uint32_t (&v)
   dequant8(w.hi.w, s2, b2, v + 28);
 }
 
+// Pass 1: rows r0, r0 + step, ... of a staged unit, each token's 256 outputs
+// scaled by its routing weight and added into y_acc with 16-byte vector
+// reductions (512 contiguous bytes per warp instruction).
+__device__ __forceinline__ void add_rows(const GemmArgs& a, const Ctl& ctl, const float* stg,
+                                         uint32_t db, const Unit& U, int r0, int step, int lane) {
+  for (int row = r0; row < U.rows; row += step) {
+    const int tj = ctl.e_tok[db][row];
+    if (tj < 0) continue;
+    const float w = ctl.e_w[db][row];
+    const float4* rp = reinterpret_cast<const float4*>(stg + row * kStageRow);
+    float* dst = a.y_acc + static_cast<size_t>(tj) * a.d + 256 * U.p + 4 * lane;
+    const float4 v0 = rp[lane], v1 = rp[32 + lane];
+    red_add_v4_f32(dst, v0.x * w, v0.y * w, v0.z * w, v0.w * w);
+    red_add_v4_f32(dst + 128, v1.x * w, v1.y * w, v1.z * w, v1.w * w);
+  }
+}
+
 template <int MODE, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     q4_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB,
@@ -294,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.drain2, 1);
     mbar_init(&ctl.d_empty[0], kEpiWarps);
     mbar_init(&ctl.d_empty[1], kEpiWarps);
-    mbar_init(&ctl.epi_bar, kEpiWarps);
+    mbar_init(&ctl.epi_bar, MODE == 0 ? kEpiWarps : kEpiWarps + kProdWarps - kProdWarpsDown);
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
     ctl.zero = 0;
@@ -324,7 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int total = n_rt * a.n_fb + a.n_sh_tiles * a.n_fb_sh;
 
-  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
+  // pass 1 needs fewer token-row copies (16-row tiles) and more hands for the
+  // row reductions: there the last four producer warps add rows instead
+  constexpr int kProd = MODE == 0 ? kProdWarps : kProdWarpsDown;
+  constexpr int kRowWarps = MODE == 0 ? kEpiWarps : kEpiWarps + kProdWarps - kProdWarpsDown;
+  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProd) {
     // ---------------------------------------------------- token-row producers
     const int pw = warp - kProdWarp0;
     const bool lead = pw == 0 && lane == 0;   // expect_tx, L2 prefetch, error reports
@@ -350,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* mB = U.shared ? &tmB_sh : &tmB;
       // this lane's token-row copy for each chunk of the unit (at most one)
       const int nops = MODE == 0 ? npad / 4 : npad / 16;
-      const int g = kProdWarps * lane + pw;
+      const int g = kProd * lane + pw;
       const bool has_op = g < nops;
       int r4[4] = {0, 0, 0, 0};
       if (has_op) {
@@ -395,6 +417,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t jp = ip - i;
         mbar_wait(&ctl.b_full[jp % kBSlots], (jp / kBSlots) & 1u, &ctl.zero, 20000000ull);
       }
+    }
+  } else if (MODE == 1 && warp >= kProdWarp0 + kProd && warp < kProdWarp0 + kProdWarps) {
+    // -------------------------------------------- row-reduction helpers (pass 1)
+    // Follow the epilogue unit by unit: once its warps have staged a unit's
+    // outputs (second barrier of the unit), add this warp's share of the rows.
+    const int hq = kEpiWarps + (warp - kProdWarp0 - kProd);   // row phase 4..7
+    const float* stg = reinterpret_cast<const float*>(sEpi);
+    uint32_t gs_phase = 0, nu = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      Unit U;
+      if (!decode_unit<NMAX>(a, n_rt, u, U)) continue;
+      if (!epi_sync(ctl, gs_phase, lim) || !epi_sync(ctl, gs_phase, lim)) {
+        if (lane == 0) raise_abort(ctl, a.err);
+        break;
+      }
+      add_rows(a, ctl, stg, nu & 1u, U, hq, kRowWarps, lane);
+      ++nu;
     }
   } else if (warp >= kMmaWarp0) {
     // ------------------------------------------------------------ MMA issuers
@@ -651,19 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) raise_abort(ctl, a.err);
           break;
         }
-        // warp q adds rows q, q+4, ...: each lane scales two 16-byte words of the
-        // row and adds them with vector reductions (512 contiguous bytes per
-        // warp instruction)
-        for (int row = q; row < U.rows; row += kEpiWarps) {
-          const int tj = ctl.e_tok[db][row];
-          if (tj < 0) continue;
-          const float w = ctl.e_w[db][row];
-          const float4* rp = reinterpret_cast<const float4*>(stg + row * kStageRow);
-          float* dst = a.y_acc + static_cast<size_t>(tj) * a.d + 256 * U.p + 4 * lane;
-          const float4 v0 = rp[lane], v1 = rp[32 + lane];
-          red_add_v4_f32(dst, v0.x * w, v0.y * w, v0.z * w, v0.w * w);
-          red_add_v4_f32(dst + 128, v1.x * w, v1.y * w, v1.z * w, v1.w * w);
-        }
+        // the epilogue and helper warps add rows q, q + kRowWarps, ...
+        add_rows(a, ctl, stg, db, U, q, kRowWarps, lane);
       }
       ++nu;
     }
