@@ -51,4 +51,32 @@ __host__ __device__ inline uint32_t bf16_pair(uint16_t v) {
   return static_cast<uint32_t>(v) | (static_cast<uint32_t>(v) << 16);
 }
 
+// Packed words of one K-chunk of one weight row (kernel-native block layout):
+// codes of K 0-31 at roff, K 32-63 at roff + 2048, scale|bias word at soff.
+struct ChunkWords {
+  uint4 lo, hi;
+  uint32_t sb;
+};
+
+__device__ __forceinline__ void load_chunk(const uint8_t* blk, uint32_t roff, uint32_t soff,
+                                           ChunkWords& w) {
+  w.lo = ld_nc_v4(blk + roff);
+  w.hi = ld_nc_v4(blk + roff + 2048);
+  w.sb = ld_nc_u32(blk + soff);
+}
+
+// 64 codes -> 32 bf16x2 words in K order.
+__device__ __forceinline__ void dequant_chunk(const ChunkWords& w, uint32_t (&v)[32]) {
+  const uint32_t s2 = bf16_pair(static_cast<uint16_t>(w.sb & 0xFFFFu));
+  const uint32_t b2 = bf16_pair(static_cast<uint16_t>(w.sb >> 16));
+  dequant8(w.lo.x, s2, b2, v + 0);
+  dequant8(w.lo.y, s2, b2, v + 4);
+  dequant8(w.lo.z, s2, b2, v + 8);
+  dequant8(w.lo.w, s2, b2, v + 12);
+  dequant8(w.hi.x, s2, b2, v + 16);
+  dequant8(w.hi.y, s2, b2, v + 20);
+  dequant8(w.hi.z, s2, b2, v + 24);
+  dequant8(w.hi.w, s2, b2, v + 28);
+}
+
 }  // namespace moeq4

@@ -234,33 +234,6 @@ __device__ __forceinline__ void prefetch_unit(const GemmArgs& a, const Unit& U) 
                      static_cast<uint32_t>(min(4, nch - c) * kPackChunkBytes));
 }
 
-// Packed words of one K-chunk for one lane: codes of K 0-31 and 32-63, scale|bias.
-struct ChunkWords {
-  uint4 lo, hi;
-  uint32_t sb;
-};
-
-__device__ __forceinline__ void load_chunk(const uint8_t* blk, uint32_t roff, uint32_t soff,
-                                           ChunkWords& w) {
-  w.lo = ld_nc_v4(blk + roff);
-  w.hi = ld_nc_v4(blk + roff + 2048);
-  w.sb = ld_nc_u32(blk + soff);
-}
-
-// 64 codes -> 32 bf16x2 words in K order.
-__device__ __forceinline__ void dequant_chunk(const ChunkWords& w, uint32_t (&v)[32]) {
-  const uint32_t s2 = bf16_pair(static_cast<uint16_t>(w.sb & 0xFFFFu));
-  const uint32_t b2 = bf16_pair(static_cast<uint16_t>(w.sb >> 16));
-  dequant8(w.lo.x, s2, b2, v + 0);
-  dequant8(w.lo.y, s2, b2, v + 4);
-  dequant8(w.lo.z, s2, b2, v + 8);
-  dequant8(w.lo.w, s2, b2, v + 12);
-  dequant8(w.hi.x, s2, b2, v + 16);
-  dequant8(w.hi.y, s2, b2, v + 20);
-  dequant8(w.hi.z, s2, b2, v + 24);
-  dequant8(w.hi.w, s2, b2, v + 28);
-}
-
 // Pass 1: rows r0, r0 + step, ... of a staged unit, each token's 256 outputs
 // scaled by its routing weight and added into y_acc with 16-byte vector
 // reductions (512 contiguous bytes per warp instruction).
