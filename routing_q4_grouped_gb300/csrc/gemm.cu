@@ -304,6 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The prologue above may overlap the previous kernel on the stream; from here
+  // on its outputs are read (block map, token rows) and written (y_acc).
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = ctl.tmem_base;
   const volatile int* abortp = &ctl.abort;
   const uint64_t lim = a.timeout_ns;
@@ -681,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // y = bf16(y_acc), eight elements per thread.
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ y_acc,
                                                        uint16_t* __restrict__ y, size_t n8) {
+  griddep_wait();   // y_acc is complete once the down pass has finished
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
     const float4 a0 = reinterpret_cast<const float4*>(y_acc)[2 * i];
@@ -709,9 +714,8 @@ cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& m, int grid, cudaStre
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  q4_grouped_gemm_kernel<MODE, NMAX><<<grid, kThreads, Lay::kSmem, s>>>(m.B, m.B_sh, m.C, m.C_sh,
-                                                                      a);
-  return cudaGetLastError();
+  return launch_pdl(q4_grouped_gemm_kernel<MODE, NMAX>, dim3(grid), dim3(kThreads), Lay::kSmem, s,
+                    m.B, m.B_sh, m.C, m.C_sh, a);
 }
 
 }  // namespace
@@ -753,8 +757,7 @@ cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStrea
   const size_t n8 = n / 8;
   if (n8 == 0) return cudaSuccess;
   int grid = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 4096));
-  finalize_kernel<<<grid, 256, 0, s>>>(y_acc, y, n8);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(grid), dim3(256), 0, s, y_acc, y, n8);
 }
 
 }  // namespace moeq4

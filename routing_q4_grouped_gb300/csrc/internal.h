@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace moeq4 {
 
 // ----------------------------------------------------------------- routing
@@ -53,6 +55,25 @@ RouteWs route_ws_layout(int T, int E, int k);
 
 // The whole routing step: one cooperative launch (sms = multiprocessors).
 cudaError_t launch_route(const RouteArgs& a, int sms, cudaStream_t s);
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on `s` finishes (it calls griddep_wait before
+// touching that kernel's data), hiding launch latency and its prologue.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Optional stage events (bench/test timing): mark(i) records event i on `s`.
 void stage_mark(int i, cudaStream_t s);

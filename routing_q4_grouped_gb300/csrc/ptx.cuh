@@ -94,6 +94,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before
+// the previous kernel on its stream has finished; it must wait here before
+// touching anything that kernel reads or writes. Returns at once for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream (if launched with the attribute) be
+// scheduled once every CTA of this grid has executed this or exited; the
+// next kernel still waits for this grid's completion in griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   int* sOff = sBase + E;               // [E+1]  expert totals, then offsets
   int* sLead = sOff + E + 1;           // [kRouteThreads] group base handed to peers
 
+  griddep_launch_dependents();   // the GEMM that follows may start its prologue
   if (tid == 0) {
     s_b = atomicAdd(&a.ctr[kCtrTicket], 1);   // virtual block id = arrival order
     s_epoch = static_cast<uint32_t>(a.ctr[kCtrEpoch]);
