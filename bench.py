@@ -175,14 +175,22 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """Largest v over the ranks (NCCL: a device tensor; gloo: a host tensor)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def layer_ids(rank, sets):
+    """Synthetic layer seeds of a rank's layer sets: every rank runs its own replica
+    on its own inputs (rank r: layers r*sets .. r*sets + sets - 1)."""
+    return [rank * sets + i for i in range(sets)]
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -262,8 +270,7 @@ def run_ours(args):
 
     # independent layer sets (weights, x, logits); rank r draws layers r*S .. r*S+S-1
     sets = []
-    for i in range(args.sets):
-        layer = rank * args.sets + i
+    for layer in layer_ids(rank, args.sets):
         W = moeq4.DeviceWeights.from_host(synth.gen_weights(cfg, layer))
         x_h = synth.gen_x(cfg, T, layer)
         l_h = synth.gen_logits(cfg, layer, T)
