@@ -4,8 +4,8 @@
     python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
                     [--workload t4096] [--block-m 128]
 
-One step = one full MoE layer call (routing, gate/up pass, down pass, bf16
-finalize) over one batch of T tokens of synthetic input already resident in
+One step = one full MoE layer call (routing, gate/up pass, down pass with the
+combine and the bf16 output) over one batch of T tokens of synthetic input already resident in
 HBM. Steps cycle through independent layer sets (weights, x, logits) whose
 weights alone exceed the 129 MB L2. Prints ONE JSON line on rank 0.
 
@@ -42,9 +42,9 @@ METRIC = "MoE-layer prefill tokens/s at T=4096; grouped-GEMM % of GB300 BF16 TC 
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # stage events 0..5 bracket: routing (one kernel; events 1 and 2 coincide), gate/up
-# GEMM, down GEMM, bf16 finalize
-STAGES = ["route", None, "gemm_gate_up_swiglu", "gemm_down_combine", "finalize_bf16"]
-LAUNCHES_PER_LAYER = 4
+# GEMM, down GEMM with the combine and the bf16 output (events 4 and 5 coincide)
+STAGES = ["route", None, "gemm_gate_up_swiglu", "gemm_down_combine", None]
+LAUNCHES_PER_LAYER = 3
 KERNEL_SOURCES = ["gemm.cu", "dequant.cuh", "ptx.cuh"]
 
 

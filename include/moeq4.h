@@ -49,10 +49,11 @@ typedef int32_t moe_status;
 /* Bits of the device error word. */
 #define MOE_DEVERR_NONFINITE_LOGIT  1  /* a router logit was NaN/Inf (treated as -inf) */
 #define MOE_DEVERR_SCAN_TIMEOUT     2  /* decoupled-lookback wait gave up */
-#define MOE_DEVERR_PIPE_TIMEOUT     4  /* a GEMM pipeline barrier wait gave up */
+#define MOE_DEVERR_PIPE_TIMEOUT     4  /* a GEMM pipeline or grid barrier wait gave up */
 #define MOE_DEVERR_BAD_TILE         8  /* a block-map entry was out of range */
-#define MOE_DEVERR_BAD_WORKSPACE   16  /* routing scratch was not zero-filled at launch, or a
-                                          row could not be placed (its write was skipped) */
+#define MOE_DEVERR_BAD_WORKSPACE   16  /* routing or FFN scratch counters were not zero at
+                                          launch, or a row could not be placed (its write
+                                          was skipped) */
 
 /* One 4-bit groupwise-affine matrix [R][K] ([A] §5-1; [C] glossary):
  *   qw    uint32 [R][K/8]   8 codes per word, code c of a row in word c/8 at bits 4*(c%8)
@@ -140,9 +141,10 @@ int32_t moe_route_max_tiles(int32_t T, int32_t E, int32_t k, int32_t block_m);
  * first use; every moe_route call leaves it zero-filled again. */
 size_t moe_route_workspace_size(int32_t T, int32_t E, int32_t k);
 
-/* Bytes of scratch for moe_expert_ffn (no zero-fill requirement): the SwiGLU
- * activations of every routed row (tile-padded to 16 rows), those of the shared
- * expert, and the fp32 combine buffer [T][d]. */
+/* Bytes of scratch for moe_expert_ffn: two grid-barrier counters (256 bytes),
+ * the SwiGLU activations of every routed row (tile-padded to 16 rows), those of
+ * the shared expert, and the fp32 combine buffer [T][d]. Zero-fill it before
+ * first use; every call leaves the counters zero again. */
 size_t moe_ffn_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
                               int32_t f_s, int32_t block_m);
 

@@ -42,9 +42,9 @@ moe_status moe_debug_tmem_layout(uint32_t* out, void* stream);
 
 /* Stage timing for benchmarks: with n > 0, moe_route / moe_expert_ffn /
  * moe_layer record events[i] (cudaEvent_t handles created by the caller) on
- * the call's stream at stage boundaries: 0 before routing, 1 after selection +
- * lookback scan, 2 after the scatter, 3 after the gate/up pass, 4 after the
- * down pass, 5 after the bf16 finalize. n = 0 turns it off. Process-wide;
+ * the call's stream at stage boundaries: 0 before routing, 1 and 2 after the
+ * routing kernel, 3 after the gate/up pass, 4 and 5 after the down pass (which
+ * also writes the bf16 output). n = 0 turns it off. Process-wide;
  * not for concurrent use from several threads. */
 moe_status moe_debug_set_stage_events(void* const* events, int32_t n);
 

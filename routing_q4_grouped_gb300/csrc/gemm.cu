@@ -251,6 +251,61 @@ __device__ __forceinline__ void add_rows(const GemmArgs& a, const Ctl& ctl, cons
   }
 }
 
+// y[i..i+7] = bf16(y_acc[i..i+7]), round to nearest even.
+__device__ __forceinline__ void bf16_store8(const float* y_acc, uint16_t* y, size_t i) {
+  const float4 a0 = reinterpret_cast<const float4*>(y_acc)[2 * i];
+  const float4 a1 = reinterpret_cast<const float4*>(y_acc)[2 * i + 1];
+  uint4 o;
+  o.x = bf16x2_bits(a0.x, a0.y);
+  o.y = bf16x2_bits(a0.z, a0.w);
+  o.z = bf16x2_bits(a1.x, a1.y);
+  o.w = bf16x2_bits(a1.z, a1.w);
+  reinterpret_cast<uint4*>(y)[i] = o;
+}
+
+// End of the down pass: once every CTA's row reductions into y_acc have been
+// performed (fence, then a bounded grid barrier: the grid has one CTA per
+// multiprocessor, so all of them run at once), each CTA converts its slice of
+// y_acc to the bf16 output. The last CTA to leave resets the counters.
+__device__ __forceinline__ void finalize_after_barrier(const GemmArgs& a, int tid) {
+  __shared__ int s_ok;
+  __threadfence();   // this thread's reductions are performed before the arrival
+  __syncthreads();
+  if (tid == 0) {
+    const int old = atomicAdd(&a.gbar[0], 1);
+    bool ok = old < static_cast<int>(gridDim.x);
+    if (!ok) atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);   // counters not zero at launch
+    uint64_t t0 = 0;
+    for (uint32_t i = 1; ok; ++i) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.gbar) : "memory");
+      if (static_cast<int>(v) >= static_cast<int>(gridDim.x)) break;
+      if ((i & 15u) == 0) {
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > a.timeout_ns) {
+          atomicOr(a.err, MOE_DEVERR_PIPE_TIMEOUT);
+          ok = false;
+        }
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (s_ok) {
+    const size_t n8 = static_cast<size_t>(a.T) * a.d / 8;
+    const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + tid; i < n8; i += stride)
+      bf16_store8(a.y_acc, a.y, i);
+  }
+  __syncthreads();
+  if (tid == 0 && atomicAdd(&a.gbar[1], 1) == static_cast<int>(gridDim.x) - 1) {
+    a.gbar[0] = 0;
+    a.gbar[1] = 0;
+  }
+}
+
 template <int MODE, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     q4_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB,
@@ -680,27 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// y = bf16(y_acc), eight elements per thread.
-__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ y_acc,
-                                                       uint16_t* __restrict__ y, size_t n8) {
-  griddep_wait();   // y_acc is complete once the down pass has finished
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
-    const float4 a0 = reinterpret_cast<const float4*>(y_acc)[2 * i];
-    const float4 a1 = reinterpret_cast<const float4*>(y_acc)[2 * i + 1];
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(a0.x, a0.y);
-    __nv_bfloat162 p1 = __floats2bfloat162_rn(a0.z, a0.w);
-    __nv_bfloat162 p2 = __floats2bfloat162_rn(a1.x, a1.y);
-    __nv_bfloat162 p3 = __floats2bfloat162_rn(a1.z, a1.w);
-    uint4 o;
-    o.x = *reinterpret_cast<uint32_t*>(&p0);
-    o.y = *reinterpret_cast<uint32_t*>(&p1);
-    o.z = *reinterpret_cast<uint32_t*>(&p2);
-    o.w = *reinterpret_cast<uint32_t*>(&p3);
-    reinterpret_cast<uint4*>(y)[i] = o;
-  }
+  if (MODE == 1) finalize_after_barrier(a, tid);
 }
 
 template <int MODE, int NMAX>
@@ -729,6 +764,8 @@ int act_rows_capacity(int T, int k, int max_tiles) {
 FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles) {
   FfnWs w{};
   size_t o = 0;
+  w.ctr = o;
+  o = 256;
   w.act = o;
   o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(act_rows_capacity(T, k, max_tiles)) * f, 256);
   w.act_sh = o;
@@ -753,11 +790,5 @@ cudaError_t launch_gemm(int mode, int tile_rows, const GemmArgs& a, const GemmMa
   return mode == 0 ? launch_mode<0, 128>(a, m, grid, s) : launch_mode<1, 128>(a, m, grid, s);
 }
 
-cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStream_t s) {
-  const size_t n8 = n / 8;
-  if (n8 == 0) return cudaSuccess;
-  int grid = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 4096));
-  return launch_pdl(finalize_kernel, dim3(grid), dim3(256), 0, s, y_acc, y, n8);
-}
 
 }  // namespace moeq4

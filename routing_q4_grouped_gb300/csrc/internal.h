@@ -138,6 +138,8 @@ struct GemmArgs {
   const uint8_t* pk;        // packed routed matrix of this pass
   const uint8_t* pk_sh;     // packed shared-expert matrix of this pass
   float* y_acc;             // [T][d] fp32 combine buffer (zeroed by pass 0)
+  uint16_t* y;              // pass 1: bf16 output y = bf16(y_acc), written after a grid barrier
+  int32_t* gbar;            // pass 1: [2] barrier arrivals and departures (zero between calls)
   int32_t* err;
   uint64_t timeout_ns;
 };
@@ -156,7 +158,7 @@ __host__ __device__ inline int act_tile_base(int row0, int ti) {
 int act_rows_capacity(int T, int k, int max_tiles);
 
 struct FfnWs {
-  size_t act, act_sh, y_acc, total;
+  size_t ctr, act, act_sh, y_acc, total;   // ctr: grid-barrier counters of the down pass
 };
 FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles);
 
@@ -165,7 +167,6 @@ FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles);
 cudaError_t launch_gemm(int mode, int tile_rows, const GemmArgs& a, const GemmMaps& m, int grid,
                         cudaStream_t s);
 
-cudaError_t launch_finalize(const float* y_acc, uint16_t* y, size_t n, cudaStream_t s);
 
 size_t gemm_smem_bytes();
 // Max rows per unit and rows per shared-expert tile for a block map of at most
