@@ -234,6 +234,19 @@ __device__ __forceinline__ void prefetch_unit(const GemmArgs& a, const Unit& U) 
                      static_cast<uint32_t>(min(4, nch - c) * kPackChunkBytes));
 }
 
+// Pass 1: copy one accumulator's npad columns (tokens) of this warp's 32 TMEM
+// lanes (features) into the token-major staging rows: col points at this
+// thread's feature of token 0, rows kStageRow floats apart.
+__device__ __forceinline__ void stage_acc(uint32_t taddr, float* col, int npad) {
+  for (int cc = 0; cc * 32 < npad; ++cc) {
+    uint32_t dv[32];
+    tmem_ld_32x32b_x32(taddr + cc * 32, dv);
+    tmem_ld_wait();   // only stores (ordered by the wait's memory clobber) follow
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) col[(cc * 32 + jj) * kStageRow] = __uint_as_float(dv[jj]);
+  }
+}
+
 // Pass 1: rows r0, r0 + step, ... of a staged unit, each token's 256 outputs
 // scaled by its routing weight and added into y_acc with 16-byte vector
 // reductions (512 contiguous bytes per warp instruction).
@@ -451,16 +464,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (MODE == 1 && warp >= kProdWarp0 + kProd && warp < kProdWarp0 + kProdWarps) {
-    // -------------------------------------------- row-reduction helpers (pass 1)
-    // Follow the epilogue unit by unit: once its warps have staged a unit's
-    // outputs (second barrier of the unit), add this warp's share of the rows.
+    // --------------------------------------- accumulator-1 and row helpers (pass 1)
+    // Follow the epilogue unit by unit: copy accumulator 1 (this warp's TMEM lane
+    // quarter, warp % 4) into the staging rows while the epilogue warps copy
+    // accumulator 0, then add this warp's share of the staged rows.
     const int hq = kEpiWarps + (warp - kProdWarp0 - kProd);   // row phase 4..7
-    const float* stg = reinterpret_cast<const float*>(sEpi);
+    const int q = warp & 3;
+    const uint32_t taddr_q = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    float* stg = reinterpret_cast<float*>(sEpi);
     uint32_t gs_phase = 0, nu = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       Unit U;
       if (!decode_unit<NMAX>(a, n_rt, u, U)) continue;
-      if (!epi_sync(ctl, gs_phase, lim) || !epi_sync(ctl, gs_phase, lim)) {
+      if (!epi_sync(ctl, gs_phase, lim) ||
+          !__all_sync(kFull, mbar_wait(&ctl.d_full, nu & 1u, abortp, lim))) {
+        if (lane == 0) raise_abort(ctl, a.err);
+        break;
+      }
+      tc_fence_after();
+      stage_acc(taddr_q + kDCol + NMAX, stg + 128 + 32 * q + lane, (U.rows + 15) & ~15);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.d_empty[1]);
+      if (!epi_sync(ctl, gs_phase, lim)) {
         if (lane == 0) raise_abort(ctl, a.err);
         break;
       }
@@ -704,20 +730,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // them at once; the next unit's MMAs start while this unit's rows are
         // scaled by their routing weight and added into y_acc, one asynchronous
         // 1 KB bulk reduction per token row.
+        // accumulator 0 here, accumulator 1 by the helper warps at the same time
         float* stg = reinterpret_cast<float*>(sEpi);
-        for (int jt = 0; jt < 2; ++jt) {
-          float* col = stg + 128 * jt + 32 * q + lane;       // this thread's feature column
-          for (int cc = 0; cc * 32 < npad; ++cc) {
-            uint32_t dv[32];
-            tmem_ld_32x32b_x32(taddr_q + kDCol + NMAX * jt + cc * 32, dv);
-            tmem_ld_wait();   // only stores (ordered by the wait's memory clobber) follow
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) col[(cc * 32 + jj) * kStageRow] = __uint_as_float(dv[jj]);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.d_empty[jt]);
-        }
+        stage_acc(taddr_q + kDCol, stg + 32 * q + lane, npad);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.d_empty[0]);
         if (!epi_sync(ctl, gs_phase, lim)) {   // every feature column of the staging rows written
           if (lane == 0) raise_abort(ctl, a.err);
           break;
