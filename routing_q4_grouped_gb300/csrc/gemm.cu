@@ -197,7 +197,15 @@ __device__ __forceinline__ bool epi_sync(Ctl& ctl, uint32_t& phase, uint64_t lim
   return ok;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+// silu(g) = g sigmoid(g) = h (1 + tanh(h)) with h = g / 2: one special-function
+// instruction per value (the hardware tanh approximation, relative error below
+// 2^-10, well under the bf16 rounding of the activation that follows).
+__device__ __forceinline__ float silu_f(float g) {
+  const float h = 0.5f * g;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
 
 // (lo, hi) -> bf16x2 bits, each rounded to nearest even, lo in the low half.
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
