@@ -49,6 +49,18 @@ def test_tiny_ragged_with_shared(T):
     _run(cfg, T=T)
 
 
+def test_tiny_large_scales():
+    # scales of 0.3-0.6, far above the synthetic recipe's 0.004-0.008
+    cfg = synth.CONFIGS["tiny"]
+    W = synth.gen_weights(cfg)
+    W = dataclasses.replace(W, **{n: O.to_bf16(O.bf16_value(getattr(W, n)) * 75.0)
+                                  for n in ("gu_scale", "dn_scale", "gu_bias", "dn_bias")})
+    x = synth.gen_x(cfg)
+    logits = synth.gen_logits(cfg)
+    y, _ = _layer_gpu(cfg, W, x, logits)
+    assert_y_close(y, O.expert_ffn(x, W, O.route(logits, cfg.k, 128)))
+
+
 def test_tiny_small_block_map():
     _run(synth.CONFIGS["tiny"], block_m=16)
 

@@ -68,6 +68,24 @@ def test_dequant_hand_groups():
     assert np.array_equal(O.bf16_value(got[0]), codes[0].astype(np.float64))
 
 
+def test_dequant_scale_range():
+    # scales from subnormal to 8 in magnitude, both signs, and zero: the
+    # in-register expansion bit-exact against the oracle
+    rng = np.random.default_rng(21)
+    rows, K = 64, 512
+    codes = rng.integers(0, 16, size=(rows, K), dtype=np.uint8)
+    qw = O.pack_codes(codes)
+    g = rows * K // 64
+    expo = rng.integers(0, 131, size=g)                     # bf16 exponent field 0..130
+    s = ((rng.integers(0, 2, size=g) << 15) | (expo << 7) | rng.integers(0, 128, size=g))
+    s[:8] = [0x0000, 0x8000, 0x3E7F, 0x3E80, 0xBE7F, 0xBE80, 0x0001, 0x3F80]   # 2^-2 edges, subnormal
+    b = O.to_bf16(rng.standard_normal(g) * 0.05)
+    s = s.astype(np.uint16).reshape(rows, -1)
+    b = np.asarray(b, np.uint16).reshape(rows, -1)
+    got = _dequant_gpu(qw, s, b)
+    assert np.array_equal(got, O.to_bf16(O.dequant(qw, s, b)).reshape(got.shape))
+
+
 def test_tmem_16x256b_fragment_layout():
     """Thread t of warp q, repetition j: registers 4j, 4j+1 hold lane base + t/4 at
     columns 8j + 2(t%4) + {0, 1}; registers 4j+2, 4j+3 hold lane base + 8 + t/4."""
