@@ -523,10 +523,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bs = ip % kBSlots;
         const uint64_t bd = bdesc0 + static_cast<uint64_t>(bs) * (kSlotBytes >> 4);
         const uint32_t ps = ip % kPairStages;
-        ok = __all_sync(kFull, mbar_wait(&ctl.ready[ps], (ip / kPairStages) & 1u, abortp, lim)) &&
-             __all_sync(kFull, mbar_wait(&ctl.b_full[bs], (ip / kBSlots) & 1u, abortp, lim));
-        if (ok && pi == 0)   // the epilogue must have read this accumulator
-          ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[j], (nu & 1u) ^ 1u, abortp, lim));
+        const uint32_t pr = (ip / kPairStages) & 1u, pb = (ip / kBSlots) & 1u;
+        const uint32_t pd = (nu & 1u) ^ 1u;
+        // The token rows (and, at a unit start, the accumulator: the epilogue
+        // must have read it) are probed before the stage wait so that the
+        // probes' latency overlaps it; whichever was not yet complete is then
+        // waited for. One vote instead of one per barrier.
+        const bool bf = mbar_test(&ctl.b_full[bs], pb);
+        const bool de = pi != 0 || mbar_test(&ctl.d_empty[j], pd);
+        ok = __all_sync(kFull, mbar_wait(&ctl.ready[ps], pr, abortp, lim) && bf && de);
+        if (!ok) {
+          ok = __all_sync(kFull, mbar_wait(&ctl.ready[ps], pr, abortp, lim)) &&
+               __all_sync(kFull, mbar_wait(&ctl.b_full[bs], pb, abortp, lim));
+          if (ok && pi == 0)
+            ok = __all_sync(kFull, mbar_wait(&ctl.d_empty[j], pd, abortp, lim));
+        }
         if (!ok) break;
         tc_fence_after();
         const uint32_t a0 = tmem + 2 * ps * kACols + 32 * j;
