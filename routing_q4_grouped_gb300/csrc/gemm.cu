@@ -614,15 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t t = tq + ps * (2 * kACols);
-      uint32_t v[32];
-      dequant_chunk(n0, v);
+      dequant_store_chunk(n0, t);
       if (more) load_chunk(pb, roff, soff, n0);
-      tmem_st_32x32b_x16(t, *reinterpret_cast<const uint32_t(*)[16]>(v));
-      tmem_st_32x32b_x16(t + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
-      dequant_chunk(n1, v);
+      dequant_store_chunk(n1, t + kACols);
       if (more) load_chunk(pb + kPackChunkBytes, roff, soff, n1);
-      tmem_st_32x32b_x16(t + kACols, *reinterpret_cast<const uint32_t(*)[16]>(v));
-      tmem_st_32x32b_x16(t + kACols + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
