@@ -173,7 +173,7 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  * such as a serving process that reserves all device memory up front and hands
  * out fixed arenas, or a plugin that has no access to its host framework's
  * allocator. Same inputs, outputs and results as moe_route, but its scratch is
- * a fixed array inside the library (about 1 MB, held on every GPU that loads
+ * a fixed array inside the library (about 2 MB, held on every GPU that loads
  * the library until the process exits), so:
  *  - sizes are limited to T <= 8192, E <= 256, k <= 8; larger ones return
  *    MOE_ERR_TOO_LARGE and enqueue nothing;
