@@ -194,14 +194,17 @@ moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void
  *   W   layer weights in the kernel-native layout (moe_q4_prepack); W->d must equal d
  *   r   routing result of moe_route for the same T (device arrays)
  *   y   bf16 [T][d] output (device)
- *   ws  scratch of moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m) bytes */
+ *   ws  scratch of moe_ffn_workspace_size(T, E, k, d, f, f_s, block_m) bytes
+ * T = 0 is allowed: nothing is launched, and x and y may be NULL. */
 moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed* W,
                           const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream);
 
 /* moe_route followed by moe_expert_ffn on the same stream, no host sync.
  *   x bf16 [T][d], logits fp32 [T][E]; r receives the routing result; y bf16 [T][d].
- *   ws of moe_layer_workspace_size(...) bytes, zero-filled before first use. */
+ *   ws of moe_layer_workspace_size(...) bytes, zero-filled before first use.
+ * T = 0 is allowed (the routing result is the empty one; x, logits and y may
+ * be NULL). */
 moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_packed* W,
                      const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                      void* stream);

@@ -184,7 +184,7 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
   moe_status st = check_route_out(r);
   if (st != MOE_OK) return st;
   if ((st = check_packed(W)) != MOE_OK) return st;
-  if (!x || !y || !ws) return MOE_ERR_ARG;
+  if ((T > 0 && (!x || !y)) || !ws) return MOE_ERR_ARG;   // x, y may be NULL when T == 0
   if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_ALIGN;
   if (T != r->T || d != W->d || W->E != r->E) return MOE_ERR_SHAPE;
   const PackLayout P = pack_layout(W->E, W->d, W->f, W->f_s);
@@ -395,7 +395,7 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
   moe_status st;
   // validate the FFN arguments before anything is enqueued
   if ((st = check_packed(W)) != MOE_OK) return st;
-  if (!x || !y) return MOE_ERR_ARG;
+  if (T > 0 && (!x || !y)) return MOE_ERR_ARG;   // x, y (and logits) may be NULL when T == 0
   if (W->E != r->E) return MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = route_impl(logits, r, ws, rsz, s)) != MOE_OK) return st;

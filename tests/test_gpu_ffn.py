@@ -99,6 +99,18 @@ def test_skew_sampled_64_row_tiles():
     _run(cfg, block_m=64, sample=np.concatenate([[0, cfg.T - 1], rng.integers(0, cfg.T, 62)]))
 
 
+def test_empty_input():
+    # T = 0: the routing result is the empty one and the FFN launches nothing;
+    # the empty x, logits and y tensors reach the library as NULL pointers
+    cfg = synth.CONFIGS["t512"]
+    W = synth.gen_weights(cfg, 0)
+    x = np.zeros((0, cfg.d), np.uint16)
+    logits = np.zeros((0, cfg.E), np.float32)
+    y, g = _layer_gpu(cfg, W, x, logits, block_m=64)
+    assert y.shape == (0, cfg.d)
+    assert_route_equal(g, O.route(logits, cfg.k, 64))
+
+
 def test_single_expert_all_rows():
     # E = k = 1: one expert group holding every token (tile tails at T % 128)
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], E=1, k=1, T=300)
