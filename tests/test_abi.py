@@ -89,3 +89,35 @@ def test_bad_arguments_rejected_on_host(L):
     inter = (E * 2 * f * d // 2 + E * 2 * f * (d // 64) * 4 + E * d * f // 2 + E * d * (f // 64) * 4
              + 2 * fs * d // 2 + 2 * fs * (d // 64) * 4 + d * fs // 2 + d * (fs // 64) * 4)
     assert L.moe_q4_packed_size(E, d, f, fs) == inter
+
+
+def test_ffn_and_layer_arguments_rejected_on_host(L):
+    lib = L.lib()
+    fake = 1 << 20                          # aligned non-null values, never dereferenced
+    r = L.RouteOutC()
+    for f in ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "n_tiles", "err"):
+        setattr(r, f, fake)
+    r.T, r.E, r.k, r.block_m = 16, 8, 2, 128
+    P = L.Q4PackedC(fake, 8, 256, 128, 0)
+    big = 1 << 30
+    ffn = lambda x, T, d, y, ws, n: lib.moe_expert_ffn(x, T, d, ctypes.byref(P), ctypes.byref(r),
+                                                      y, ws, n, None)
+    assert ffn(None, 16, 256, fake, fake, big) == -1          # x NULL with T > 0
+    assert ffn(fake, 16, 256, None, fake, big) == -1          # y NULL with T > 0
+    assert ffn(fake, 16, 256, fake, None, big) == -1          # no workspace
+    assert ffn(fake + 8, 16, 256, fake, fake, big) == -7      # x not 16-byte aligned
+    assert ffn(fake, 15, 256, fake, fake, big) == -2          # T differs from the routing result
+    assert ffn(fake, 16, 512, fake, fake, big) == -2          # d differs from the weights
+    assert ffn(fake, 16, 256, fake, fake, 64) == -3           # workspace too small
+    r.E = 16                                                  # routing over more experts than W has
+    assert ffn(fake, 16, 256, fake, fake, big) == -2
+    r.E = 8
+    lay = lambda x, lg, T, y, ws, n: lib.moe_layer(x, lg, T, ctypes.byref(P), ctypes.byref(r),
+                                                   y, ws, n, None)
+    assert lay(fake, fake, 15, fake, fake, big) == -2         # T differs from r.T
+    assert lay(fake, fake, 16, fake, None, big) == -3         # no workspace
+    assert lay(fake, fake, 16, fake, fake, 64) == -3          # workspace too small
+    assert lay(None, fake, 16, fake, fake, big) == -1         # x NULL with T > 0
+    assert lay(fake, fake, 16, None, fake, big) == -1         # y NULL with T > 0
+    r.E = 16
+    assert lay(fake, fake, 16, fake, fake, big) == -2         # expert counts differ
