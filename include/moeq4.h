@@ -12,7 +12,10 @@
  *  - All array pointers are DEVICE pointers, 16-byte aligned, owned by the
  *    caller. The library never allocates, frees or synchronises (except
  *    moe_get_device_error, which says so), and keeps no state between calls
- *    besides per-device constants (SM count, kernel attributes).
+ *    besides per-device constants (SM count) and the GEMM kernels' dynamic
+ *    shared-memory attribute, which is set once per process, on the first
+ *    device that runs the FFN: a process that runs the FFN on a second
+ *    device gets MOE_ERR_CUDA there (a known limitation).
  *  - Every compute call is asynchronous on `stream` (a cudaStream_t passed as
  *    void*; NULL = legacy default stream). Outputs are valid in stream order.
  *  - bf16 values are passed as their uint16_t bit patterns.
