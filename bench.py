@@ -13,6 +13,10 @@ Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
 layer is independent per token batch: weak scaling, no data-path collective);
 the time is the max over ranks.
 
+--workload chunked runs the chunked multi-layer prefill instead: one step is
+T = 32768 tokens in 4096-token chunks through 40 layers with their own weights
+(routing, both GEMM passes and the next-input step per chunk and layer).
+
 --impl reference times the CPU oracle (plain numpy, float64) on a bounded
 sample of the same workload on the host cores.
 """
@@ -241,13 +245,28 @@ def run_reference(args):
         times.append(t)
     sec = statistics.mean(times)
     value = T / sec
+    if cfg.layers > 1:
+        # the chunked run: one chunk-layer timed (plus the oracle's next-input
+        # step), extrapolated to every layer of every chunk
+        import oracle as O
+
+        x = synth.gen_x(cfg, T)
+        t0 = time.perf_counter()
+        O.rms_unit(x, x)
+        t_rms = time.perf_counter() - t0
+        n_chunks = cfg.T // T
+        sec = (sec + t_rms) * cfg.layers * n_chunks
+        value = cfg.T / sec
+        note = (f"{note}; that chunk-layer (with the next-input step) extrapolated to "
+                f"{cfg.layers} layers x {n_chunks} chunks")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator, same recipe as the GPU arm)",
-        "config": {"workload": args.workload, "T": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
-                   "f": cfg.f, "f_s": cfg.f_s, "block_m": args.block_m},
+        "config": {"workload": args.workload, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+                   "f": cfg.f, "f_s": cfg.f_s, "block_m": args.block_m,
+                   **({"chunk": cfg.chunk, "layers": cfg.layers} if cfg.layers > 1 else {})},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "per step: " + note},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -448,6 +467,213 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- chunked multi-layer run
+
+
+def device_q4_layer(cfg, gen, device="cuda"):
+    """One layer's 4-bit weights in the interchange layout, drawn on `device` from
+    the seeded torch generator `gen` with the synthetic recipe (uniform codes;
+    scale ~ U(0.004, 0.008) -> bf16; bias = -7.5 scale + N(0, 0.001) -> bf16).
+    The chunked run holds 40 layers (18 GB); drawing them on the host takes
+    minutes, and the timing does not depend on which random values they hold.
+    Returns {name: tensor} with the names DeviceWeights uses."""
+    import torch
+
+    def mat(prefix, experts, rows, K):
+        qw = torch.randint(0, 1 << 32, (experts, rows, K // 8), dtype=torch.int64,
+                           generator=gen, device=device).to(torch.int32)   # wraps to 32 bits
+        shp = (experts, rows, K // 64)
+        s = (0.004 + 0.004 * torch.rand(shp, generator=gen, device=device)).to(torch.bfloat16)
+        b = (-7.5 * s.float() + 0.001 * torch.randn(shp, generator=gen, device=device)).to(torch.bfloat16)
+        return {prefix + "_qw": qw, prefix + "_scale": s.view(torch.int16),
+                prefix + "_bias": b.view(torch.int16)}
+
+    E, d, f, fs = cfg.E, cfg.d, cfg.f, cfg.f_s
+    ts = {**mat("gu", E, 2 * f, d), **mat("dn", E, d, f)}
+    if fs:
+        ts.update(mat("sgu", 1, 2 * fs, d))
+        ts.update(mat("sdn", 1, d, fs))
+    return ts
+
+
+def run_chunked(args):
+    """One step = the whole chunked run: every chunk of `cfg.chunk` tokens goes
+    through all `cfg.layers` layers (routing, gate/up pass, down pass, then the
+    next input bf16(rms_unit(y + x))), each layer with its own weights, all
+    resident in HBM. `value` = tokens of the whole run / step time."""
+    import torch
+
+    from routing_q4_grouped_gb300 import moeq4
+
+    world, rank, local = dist_setup()
+    from routing_q4_grouped_gb300 import synth
+
+    cfg = synth.CONFIGS[args.workload]
+    C, L = cfg.chunk, cfg.layers
+    nch = cfg.T // C
+    d, E, k, f, fs = cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_s
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1_000_003 * cfg.seed + rank)
+    layers = []
+    for _ in range(L):
+        dw = moeq4.DeviceWeights(E, d, f, fs, device_q4_layer(cfg, gen))
+        dw.packed = torch.empty(moeq4.moe_q4_packed_size(E, d, f, fs), dtype=torch.uint8,
+                                device="cuda")
+        moeq4.moe_q4_prepack(dw, dw.packed)
+        stream.synchronize()
+        dw.tensors = {}
+        layers.append(dw)
+    x0 = torch.randn((nch, C, d), generator=gen, device="cuda").to(torch.bfloat16)
+    logits = torch.randn((nch, L, C, E), generator=gen, device="cuda")   # chunk-major
+    route = moeq4.RouteBuffers.alloc(C, E, k, args.block_m)
+    ws = moeq4.alloc_workspace(moeq4.moe_layer_workspace_size(C, E, k, d, f, fs, args.block_m))
+    y = torch.empty((C, d), dtype=torch.bfloat16, device="cuda")
+    xb = [torch.empty((C, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    out = torch.empty((nch, C, d), dtype=torch.bfloat16, device="cuda")
+
+    def run_chunk(x_in, lg, y_out):
+        # layers 0..L-1 of one chunk; the last layer writes the chunk's output
+        cur = x_in
+        for l in range(L):
+            last = l + 1 == L
+            moeq4.moe_layer(cur, lg[l], layers[l], route, y_out if last else y, ws, stream)
+            if not last:
+                nxt = xb[l % 2]
+                moeq4.moe_residual_rms(y, cur, nxt, stream)
+                cur = nxt
+
+    def step():
+        for c in range(nch):
+            run_chunk(x0[c], logits[c], out[c])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if moeq4.moe_get_device_error(route) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    clocks = ClockSampler(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
+    ms_step = ms_total / args.steps
+    value = cfg.T * world * args.steps / (ms_total * 1e-3)
+
+    # gate/up kernel times over the first chunk's layers (stage events)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(L)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    cur = x0[0]
+    for l in range(L):
+        moeq4.moe_debug_set_stage_events(evs[l])
+        moeq4.moe_layer(cur, logits[0, l], layers[l], route, y, ws, stream)
+        moeq4.moe_debug_set_stage_events([])
+        if l + 1 < L:
+            moeq4.moe_residual_rms(y, cur, xb[l % 2], stream)
+            cur = xb[l % 2]
+    torch.cuda.synchronize()
+    kern = {s: statistics.mean(evs[l][j].elapsed_time(evs[l][j + 1]) for l in range(L))
+            for j, s in enumerate(STAGES) if s}
+
+    # end to end: every step copies x and all logits in from pinned host memory
+    # (one copy each, on a host->device stream; chunk c waits for its inputs) and
+    # every chunk's output back (device->host stream)
+    x_h = x0.view(torch.int16).cpu().pin_memory()
+    lg_h = logits.cpu().pin_memory()
+    out_h = torch.empty((nch, C, d), dtype=torch.int16).pin_memory()
+    x_d, lg_d = torch.empty_like(x0), torch.empty_like(logits)
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_step():
+        ready = []
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_stream(stream)          # the previous step no longer reads x_d, lg_d
+            for c in range(nch):
+                x_d[c].view(torch.int16).copy_(x_h[c], non_blocking=True)
+                lg_d[c].copy_(lg_h[c], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(h2d_s)
+                ready.append(e)
+        stream.wait_stream(d2h_s)              # the previous step's outputs have left `out`
+        for c in range(nch):
+            stream.wait_event(ready[c])
+            run_chunk(x_d[c], lg_d[c], out[c])
+            done = torch.cuda.Event()
+            done.record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done)
+                out_h[c].copy_(out[c].view(torch.int16), non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0.record(stream)
+    h2d_s.wait_event(ev0)
+    for _ in range(args.steps):
+        e2e_step()
+    fin = torch.cuda.Event()
+    fin.record(d2h_s)
+    stream.wait_event(fin)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, ev0.elapsed_time(ev1))
+    e2e_value = cfg.T * world * args.steps / (e2e_ms * 1e-3)
+    if moeq4.moe_get_device_error(route) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # roofline of the dominant kernel (gate/up at T = chunk), as in the one-layer bench
+    pk, pk_src = peaks()
+    flops_gu = 4 * d * f * C * k + 4 * d * fs * C
+    flops_dn = 2 * d * f * C * k + 2 * d * fs * C
+    t_gu, t_dn = kern["gemm_gate_up_swiglu"] * 1e-3, kern["gemm_down_combine"] * 1e-3
+    peak_tf = pk["bf16_tflops_sustained"] if "bf16_tflops_sustained" in pk else pk["bf16_tflops"]
+    roof = {"bound": "tensor", "achieved": flops_gu / t_gu / 1e12, "peak": peak_tf,
+            "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "q4_grouped_gemm_kernel<0> (gate/up + SwiGLU)"
+    roof["peak_source"] = f"{pk_src} (bf16 sustained: kernels timed inside a long run)"
+    gg_tflops = (flops_gu + flops_dn) / (t_gu + t_dn) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch generator on the device, same value recipe; random-init 4-bit weights)",
+        "config": {"workload": args.workload, "T": cfg.T, "chunk": C, "layers": L, "d": d, "E": E,
+                   "k": k, "f": f, "f_s": fs, "block_m": args.block_m,
+                   "l2": f"inputs larger than L2: {L} layers of {layers[0].nbytes / 1e6:.0f} MB weights per step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "grouped_gemm": {"tflops": gg_tflops, "frac_bf16_peak": gg_tflops / peak_tf,
+                         "ms": (t_gu + t_dn) * 1e3},
+        "kernels_ms": kern,
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": x0.numel() * 2 + logits.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2},
+        "clocks": clk,
+        "gpu_launches": (LAUNCHES_PER_LAYER * L + (L - 1)) * nch * args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     from routing_q4_grouped_gb300 import synth
@@ -459,6 +685,8 @@ def main():
         args.block_m = int(args.block_m)
     if args.impl == "reference":
         run_reference(args)
+    elif cfg.layers > 1:
+        run_chunked(args)
     else:
         run_ours(args)
 
