@@ -13,9 +13,7 @@
  *    caller. The library never allocates, frees or synchronises (except
  *    moe_get_device_error, which says so), and keeps no state between calls
  *    besides per-device constants (SM count) and the GEMM kernels' dynamic
- *    shared-memory attribute, which is set once per process, on the first
- *    device that runs the FFN: a process that runs the FFN on a second
- *    device gets MOE_ERR_CUDA there (a known limitation).
+ *    shared-memory attribute, which is set once per device.
  *  - Every compute call is asynchronous on `stream` (a cudaStream_t passed as
  *    void*; NULL = legacy default stream). Outputs are valid in stream order.
  *  - bf16 values are passed as their uint16_t bit patterns.
@@ -140,8 +138,14 @@ typedef struct moe_route_out {
 /* Upper bound on the block-map length: T*k/block_m + min(E, T*k). */
 int32_t moe_route_max_tiles(int32_t T, int32_t E, int32_t k, int32_t block_m);
 
-/* Bytes of scratch for moe_route. The buffer must be zero-filled before its
- * first use; every moe_route call leaves it zero-filled again. */
+/* Bytes of scratch for moe_route: 256 bytes of counters (block ticket, blocks
+ * done, call epoch), then the epoch-tagged lookback words of the prefix scan.
+ * Zero-fill the buffer before its first use. A call that completes leaves the
+ * ticket and done counters at zero again but advances the epoch and leaves
+ * its lookback words behind (the next call's epoch makes them stale): keep the
+ * buffer untouched between routing calls, and do not reuse it for anything
+ * that expects zeroed memory. After a call that set a device error bit,
+ * zero-fill the whole buffer again before the next call. */
 size_t moe_route_workspace_size(int32_t T, int32_t E, int32_t k);
 
 /* Bytes of scratch for moe_expert_ffn: two grid-barrier counters (256 bytes),
@@ -182,9 +186,11 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  *    MOE_ERR_TOO_LARGE and enqueue nothing;
  *  - the first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture;
- *  - every call shares the one array: each call first clears the part that
- *    must start at zero, and calls whose work overlaps on the GPU (other
- *    streams, other host threads) race and must be serialised by the caller;
+ *  - every call shares the one array: each call first clears the counters
+ *    that must start at zero and takes a new epoch, so that whatever an
+ *    earlier call left behind (even one that did not finish) is ignored; calls
+ *    whose work overlaps on the GPU (other streams, other host threads) race
+ *    and must be serialised by the caller;
  *  - it calls no cudaMalloc, cudaFree or allocating library routine. */
 moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void* stream);
 

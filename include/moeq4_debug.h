@@ -48,6 +48,11 @@ moe_status moe_debug_tmem_layout(uint32_t* out, void* stream);
  * not for concurrent use from several threads. */
 moe_status moe_debug_set_stage_events(void* const* events, int32_t n);
 
+/* Device address and size of the fixed scratch array that moe_route_noalloc
+ * uses on the current device (looked up with that device current), so that a
+ * test can plant stale contents in it. */
+moe_status moe_debug_noalloc_scratch(void** addr, size_t* bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -298,6 +298,16 @@ moe_status noalloc_scratch(void** out) {
   return MOE_OK;
 }
 
+// Opens the fixed scratch for a new call: the ticket and leave counters back to
+// zero and a fresh epoch, so that lookback words left behind by an earlier call
+// that did not finish (its blocks refused out-of-range tickets, for example after
+// two calls overlapped) carry an older epoch and read as unpublished.
+__global__ void noalloc_open_kernel(int32_t* ctr) {
+  ctr[kCtrTicket] = 0;
+  ctr[kCtrLeave] = 0;
+  ctr[kCtrEpoch] = static_cast<int32_t>(static_cast<uint32_t>(ctr[kCtrEpoch]) + 1u);
+}
+
 std::mutex g_ev_mu;
 cudaEvent_t g_events[8] = {};
 int g_nevents = 0;
@@ -413,6 +423,14 @@ moe_status moe_get_device_error(const int32_t* err, int32_t* code, void* stream)
   return v ? MOE_ERR_DEVICE : MOE_OK;
 }
 
+moe_status moe_debug_noalloc_scratch(void** addr, size_t* bytes) {
+  if (!addr || !bytes) return MOE_ERR_ARG;
+  moe_status st = noalloc_scratch(addr);
+  if (st != MOE_OK) return st;
+  *bytes = kNoAllocBytes;
+  return MOE_OK;
+}
+
 moe_status moe_debug_set_stage_events(void* const* events, int32_t n) {
   if (n < 0 || n > 8 || (n > 0 && !events)) return MOE_ERR_ARG;
   std::lock_guard<std::mutex> g(g_ev_mu);
@@ -431,9 +449,10 @@ moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the ticket and leave counters must start at zero (each call also leaves them
-  // zero); the epoch counter and the lookback words may hold anything
-  if (cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the ticket and leave counters must start at zero and the call needs an epoch
+  // of its own; the lookback words may hold anything
+  noalloc_open_kernel<<<1, 1, 0, s>>>(static_cast<int32_t*>(ws));
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   return route_impl(logits, out, ws, kNoAllocBytes, s);
 }
 

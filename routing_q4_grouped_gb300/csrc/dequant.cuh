@@ -10,7 +10,10 @@
 // this single-rounded bf16 FMA equals bf16(fp32(s)*q + fp32(b)).
 //
 // Code -> bf16: OR-ing a nibble into the mantissa of bf16 128.0 (0x4300) gives
-// exactly 128 + q; one bf16x2 subtraction of (128, 128) recovers q exactly, one
+// exactly 128 + q (the exponent-bias or "magic number" integer-to-float
+// conversion; its use with lop3 for 4-bit weights is described by Kim et al.,
+// "Who Says Elephants Can't Run: Bringing Large Scale MoE Models into Cloud
+// Scale Production", 2022, for fp16); one bf16x2 subtraction of (128, 128) recovers q exactly, one
 // bf16x2 FMA applies the affine map. The kernel-native layout stores each
 // word's nibbles in the order (k0, k2, k4, k6, k1, k3, k5, k7), so a shift and
 // one mask extract the pair (k2j, k2j+1) ready for the bf16x2 lanes.

@@ -57,6 +57,7 @@
 //   overlap the MMAs of the next.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_bf16.h>
 
@@ -789,19 +790,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (MODE == 1) finalize_after_barrier(a, tid);
 }
 
+// A kernel's dynamic shared-memory limit is an attribute of the function as
+// loaded on one device: set it once per device (with that device current).
+template <int MODE, int NMAX>
+cudaError_t set_smem_attr_once() {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static bool done[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(q4_grouped_gemm_kernel<MODE, NMAX>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Layout<MODE, NMAX>::kSmem));
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 template <int MODE, int NMAX>
 cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s) {
-  using Lay = Layout<MODE, NMAX>;
-  static bool attr_set = false;   // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(q4_grouped_gemm_kernel<MODE, NMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Lay::kSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return launch_pdl(q4_grouped_gemm_kernel<MODE, NMAX>, dim3(grid), dim3(kThreads), Lay::kSmem, s,
-                    m.B, m.B_sh, m.C, m.C_sh, a);
+  cudaError_t e = set_smem_attr_once<MODE, NMAX>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(q4_grouped_gemm_kernel<MODE, NMAX>, dim3(grid), dim3(kThreads),
+                    Layout<MODE, NMAX>::kSmem, s, m.B, m.B_sh, m.C, m.C_sh, a);
 }
 
 }  // namespace

@@ -1,7 +1,9 @@
 // prepack.cu — one-time conversion of 4-bit weights from the interchange layout
 // (codes [R][K/8] uint32, scale/bias [R][K/64] bf16) into the kernel-native
-// layout the grouped GEMM streams with one bulk copy per K-chunk. Values are
-// unchanged: only the order of rows, 16-byte halves and nibbles moves.
+// layout the grouped GEMM streams: per K-chunk of a 256-row unit one contiguous
+// block that its dequantisation warps read with 16-byte loads (and that the
+// GEMM prefetches into L2 with bulk prefetches). Values are unchanged: only
+// the order of rows, 16-byte halves and nibbles moves.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -18,7 +20,7 @@ __global__ void __launch_bounds__(256) prepack_kernel(const uint32_t* __restrict
                                                       const uint16_t* __restrict__ bias,
                                                       int experts, int R, int K, int kind,
                                                       int F_or_d, uint8_t* __restrict__ dst) {
-  const int units = kind == 0 ? R / 256 : R / 256;   // 2F/256 or d/256 units per expert
+  const int units = R / 256;   // units per expert: 2F/256 (gate/up) or d/256 (down)
   const int nch = K / 64;
   const size_t n = static_cast<size_t>(experts) * units * nch * 256;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;

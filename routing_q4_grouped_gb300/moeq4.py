@@ -78,6 +78,7 @@ _SIGS = {
     "moe_debug_mma": (_c_i32, [_c_i32, _c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr]),
     "moe_debug_set_stage_events": (_c_i32, [ctypes.POINTER(_c_ptr), _c_i32]),
     "moe_debug_tmem_layout": (_c_i32, [_c_ptr, _c_ptr]),
+    "moe_debug_noalloc_scratch": (_c_i32, [ctypes.POINTER(_c_ptr), ctypes.POINTER(_c_size)]),
 }
 
 
@@ -307,6 +308,14 @@ def moe_debug_mma(a_from_tmem: bool, A, B, D, stream=None) -> None:
 
 def moe_debug_tmem_layout(out, stream=None) -> None:
     _check("moe_debug_tmem_layout", lib().moe_debug_tmem_layout(_ptr(out), _stream(stream)))
+
+
+def moe_debug_noalloc_scratch() -> tuple[int, int]:
+    """(device address, bytes) of moe_route_noalloc's fixed scratch on the current device."""
+    addr, n = _c_ptr(), _c_size()
+    _check("moe_debug_noalloc_scratch",
+           lib().moe_debug_noalloc_scratch(ctypes.byref(addr), ctypes.byref(n)))
+    return int(addr.value), int(n.value)
 
 
 def moe_debug_set_stage_events(events) -> None:

@@ -72,8 +72,9 @@ def uniform(seed, tid, layer, n, start=0) -> np.ndarray:
     return u.astype(np.float64) * (1.0 / 9007199254740992.0)
 
 
-def normal(seed, tid, layer, n) -> np.ndarray:
-    u = uniform(seed, tid, layer, 2 * n)
+def normal(seed, tid, layer, n, start=0) -> np.ndarray:
+    """Normals [start, start+n) of the stream (normal i uses uniforms 2i, 2i+1)."""
+    u = uniform(seed, tid, layer, 2 * n, 2 * start)
     u1, u2 = u[0::2], u[1::2]
     return np.sqrt(-2.0 * np.log1p(-u1)) * np.cos(2.0 * math.pi * u2)
 
@@ -120,17 +121,20 @@ CONFIGS = {
 }
 
 
-def gen_x(cfg: Config, T: int | None = None, layer: int = 0) -> np.ndarray:
-    """Token activations, bf16 bits [T, d] (``layer`` selects an independent draw)."""
+def gen_x(cfg: Config, T: int | None = None, layer: int = 0, t0: int = 0) -> np.ndarray:
+    """Token activations, bf16 bits [T, d] of tokens t0 .. t0+T-1 (``layer``
+    selects an independent draw)."""
     T = cfg.T if T is None else T
-    return to_bf16_bits(normal(cfg.seed, TID["x"], layer, T * cfg.d).reshape(T, cfg.d))
+    d = cfg.d
+    return to_bf16_bits(normal(cfg.seed, TID["x"], layer, T * d, t0 * d).reshape(T, d))
 
 
-def gen_logits(cfg: Config, layer: int = 0, T: int | None = None) -> np.ndarray:
-    """Router logits, fp32 [T, E], following the configuration's recipe."""
+def gen_logits(cfg: Config, layer: int = 0, T: int | None = None, t0: int = 0) -> np.ndarray:
+    """Router logits, fp32 [T, E] of tokens t0 .. t0+T-1, following the
+    configuration's recipe."""
     T = cfg.T if T is None else T
     E = cfg.E
-    z = normal(cfg.seed, TID["logits"], layer, T * E).reshape(T, E)
+    z = normal(cfg.seed, TID["logits"], layer, T * E, t0 * E).reshape(T, E)
     if cfg.logits == "expert_offset":
         z = z + 0.5 * normal(cfg.seed, TID["expert_bias"], layer, E)[None, :]
     elif cfg.logits == "zipf":

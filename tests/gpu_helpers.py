@@ -54,8 +54,9 @@ def assert_route_equal(g: dict, r: O.Route):
     assert np.array_equal(g["inv"], r.inv)
     assert g["n_tiles"] == r.n_tiles
     assert np.array_equal(g["tiles"], r.tiles)
-    # weights: fp64 on both sides, one rounding to fp32 -> equal except at rounding ties
-    assert ulp_diff_f32(g["w"], r.w).max(initial=0) <= 1
+    # weights: float64 on both sides, then one rounding to fp32: bit-exact
+    assert np.array_equal(g["w"].view(np.uint32), r.w.view(np.uint32)), \
+        ulp_diff_f32(g["w"], r.w).max(initial=0)
 
 
 def assert_y_close(y_gpu: np.ndarray, y_ref: np.ndarray):

@@ -161,3 +161,72 @@ def test_chunked_three_stacked_layers():
         nxt = np.zeros_like(xr)
         nxt[tok] = O.rms_unit(yr, xr[tok])
         xr = nxt
+
+
+def test_chunked_late_chunk_teacher_forced():
+    """Chunk 7 (tokens 28672..32767) of the chunked run at layers 0, 1, 20 and
+    39, each with its own seeded weights and that chunk's rows of its logits.
+
+    Teacher forcing: both sides get the same layer input, so every layer is
+    checked on its own. Layer 0's input is the prompt's chunk; a deeper layer's
+    input is a seeded stand-in with the chain's statistics (per-token unit RMS
+    in bf16), drawn by the generator for both sides. The GPU runs the whole
+    chunk (routing bit-exact on all 4096 tokens); the oracle runs 256 sampled
+    tokens, which is exact for them because every token is independent.
+    """
+    cfg = synth.CONFIGS["chunked"]
+    C, chunk = cfg.chunk, 7
+    t0 = chunk * C
+    tok = np.unique(np.random.default_rng(71).choice(C, 256, replace=False))
+    assert tok.size == 256
+    for layer in (0, 1, 20, 39):
+        if layer == 0:
+            x = synth.gen_x(cfg, C, 0, t0)
+        else:
+            raw = O.bf16_value(synth.gen_x(cfg, C, 1000 + layer, t0))
+            x = O.to_bf16(raw / np.sqrt(np.mean(raw * raw, axis=1, keepdims=True)))
+        logits = synth.gen_logits(cfg, layer, C, t0)
+        W = synth.gen_weights(cfg, layer)
+        y, g = _layer_gpu(cfg, W, x, logits, 128)
+        r = O.route(logits, cfg.k, 128)
+        assert_route_equal(g, r)
+        assert_y_close(y[tok], O.expert_ffn(x, W, r, tokens=tok))
+
+
+def test_chunked_bench_weights():
+    """The chunked benchmark draws its 40 layers on the device with a seeded
+    torch generator (same value recipe). One such layer, copied to the host,
+    through the oracle on sampled tokens of a 4096-token chunk."""
+    import importlib.util
+    import os
+
+    spec = importlib.util.spec_from_file_location(
+        "bench_mod", os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                                  "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    cfg = synth.CONFIGS["chunked"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    ts = bench.device_q4_layer(cfg, gen)
+    host = {n: t.cpu().numpy() for n, t in ts.items()}
+    u = lambda a: a.view(np.uint32) if a.dtype == np.int32 else a.view(np.uint16)
+    W = synth.Q4Weights(cfg.E, cfg.d, cfg.f, cfg.f_s,
+                        **{n: u(a) for n, a in host.items()})
+    # the recipe's ranges hold for the device draw as well
+    s = O.bf16_value(W.gu_scale)
+    assert s.min() >= 0.004 - 2 ** -15 and s.max() <= 0.008 + 2 ** -14
+    C = cfg.chunk
+    x = synth.gen_x(cfg, C)
+    logits = synth.gen_logits(cfg, 0, C)
+    dw = moeq4.DeviceWeights(cfg.E, cfg.d, cfg.f, cfg.f_s, ts)
+    dw.packed = torch.empty(moeq4.moe_q4_packed_size(cfg.E, cfg.d, cfg.f, cfg.f_s),
+                            dtype=torch.uint8, device="cuda")
+    moeq4.moe_q4_prepack(dw, dw.packed)
+    layer = moeq4.Layer(dw, C, cfg.k, 128)
+    y = layer(dev(x), dev(logits))
+    assert moeq4.moe_get_device_error(layer.route) == 0
+    r = O.route(logits, cfg.k, 128)
+    assert_route_equal(route_np(layer.route), r)
+    tok = np.unique(np.random.default_rng(72).integers(0, C, 64))
+    assert_y_close(bits(y)[tok], O.expert_ffn(x, W, r, tokens=tok))

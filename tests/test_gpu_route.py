@@ -1,5 +1,6 @@
-"""GPU routing against the oracle: every routing/indexing output bit-exact,
-weights within one fp32 ulp, on the workloads and the edge cases."""
+"""GPU routing against the oracle: every routing output (ids, weights, counts,
+offsets, permutation, inverse, block map) bit-exact, on the workloads and the
+edge cases."""
 import numpy as np
 import pytest
 import torch

@@ -137,3 +137,23 @@ def test_rms_unit_closed_form():
     v = np.tile([1.0, -3.0], d // 2)
     out = O.rms_unit(np.zeros((1, d), np.uint16), O.to_bf16(v)[None])
     assert np.array_equal(out[0], O.to_bf16(v / np.sqrt(5.0)))
+
+
+def test_process_pool_layer_equals_the_oracle():
+    # the benchmark's CPU baseline spreads expert groups over processes; the
+    # layer it computes is the oracle's
+    from oracle.pool import OraclePool
+
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], f_s=128)
+    W = synth.gen_weights(cfg)
+    x = synth.gen_x(cfg)
+    logits = synth.gen_logits(cfg)
+    pool = OraclePool(2)
+    try:
+        pool.load(W, x)
+        r, y = pool.layer(logits, cfg.k, 16)
+    finally:
+        pool.close()
+    ref = O.expert_ffn(x, W, O.route(logits, cfg.k, 16))
+    assert np.array_equal(y, ref)
+    assert r.n_tiles > 0

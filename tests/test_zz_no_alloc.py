@@ -65,3 +65,51 @@ def test_sizes_beyond_the_fixed_scratch_are_rejected():
     with pytest.raises(moeq4.MoeError) as e:
         moeq4.moe_route_noalloc(logits, out)
     assert e.value.status == moeq4.MOE_ERR_TOO_LARGE
+
+
+def test_limit_sizes_match_workspace_routing():
+    # the largest sizes the fixed scratch is laid out for: T = 8192, E = 256, k = 8
+    rng = np.random.default_rng(8192)
+    a = torch.from_numpy(rng.standard_normal((8192, 256)).astype(np.float32)).cuda()
+    for bm in (128, 64):
+        _same(_route_noalloc(a, 8, bm), _route_ws(a, 8, bm))
+
+
+@pytest.mark.parametrize("T,E,k", [(64, 257, 2), (64, 256, 9)])
+def test_expert_and_topk_beyond_the_fixed_scratch_are_rejected(T, E, k):
+    out = moeq4.RouteBuffers.alloc(T, E, k, 128)
+    logits = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+    with pytest.raises(moeq4.MoeError) as e:
+        moeq4.moe_route_noalloc(logits, out)
+    assert e.value.status == moeq4.MOE_ERR_TOO_LARGE
+
+
+def test_words_of_an_unfinished_call_are_ignored():
+    # A call that did not finish (say, one that raced an overlapping call and
+    # had blocks refuse their tickets) leaves lookback words tagged with the
+    # epoch it ran under, some claiming inclusive prefixes, and the epoch
+    # counter not advanced. Plant exactly that state in the fixed scratch: every
+    # lookback word at the current epoch, marked inclusive with a wrong count,
+    # and dirty ticket and leave counters. The next call must start a new epoch
+    # of its own and route exactly as moe_route does.
+    cfg = synth.CONFIGS["t512"]
+    logits = torch.from_numpy(synth.gen_logits(cfg)).cuda()
+    ref = _route_ws(logits, cfg.k, 128)
+    _same(_route_noalloc(logits, cfg.k, 128), ref)
+    addr, nbytes = moeq4.moe_debug_noalloc_scratch()
+
+    class _Scratch:   # the library's array seen as an int32 tensor (no copy)
+        __cuda_array_interface__ = {"shape": (nbytes // 4,), "typestr": "<i4",
+                                    "data": (addr, False), "version": 3}
+
+    scratch = torch.as_tensor(_Scratch(), device="cuda")
+    torch.cuda.synchronize()
+    epoch = int(scratch[2])
+    scratch[0] = 5                                        # ticket counter
+    scratch[1] = 3                                        # blocks-done counter
+    words = scratch[64:].view(torch.int64)
+    word = ((epoch & 0xFFFFFFFF) << 32) | (2 << 30) | 777  # inclusive, wrong count, current epoch
+    words.fill_(word - (1 << 64) if word >= 1 << 63 else word)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        _same(_route_noalloc(logits, cfg.k, 128), ref)
