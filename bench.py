@@ -516,6 +516,61 @@ def measure_workload(name, args, world, rank, local, steps, warmup, sets_n, cloc
     }
 
 
+def measure_router(name, steps, warmup):
+    """The fused router (projection + top-k) alone and the whole layer from
+    hidden states (router, routing from its choice, expert FFN) on workload
+    `name`, with seeded router weights ~ N(0, 1/d)."""
+    import torch
+
+    from routing_q4_grouped_gb300 import moeq4, synth
+
+    cfg = synth.CONFIGS[name]
+    T, d, E, k, f, fs = cfg.tokens_per_call, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_s
+    bm = moeq4.default_block_m(T, E, k)
+    stream = torch.cuda.current_stream()
+    x = torch.from_numpy(synth.gen_x(cfg, T).view(np.int16)).cuda().view(torch.bfloat16)
+    wr = torch.from_numpy(synth.gen_router(cfg).view(np.int16)).cuda().view(torch.bfloat16)
+    W = moeq4.DeviceWeights.from_host(synth.gen_weights(cfg, 0))
+    route = moeq4.RouteBuffers.alloc(T, E, k, bm)
+    lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ws = moeq4.alloc_workspace(moeq4.moe_layer_workspace_size(T, E, k, d, f, fs, bm))
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # larger than L2
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot / steps
+
+    ms_router = timed(lambda: moeq4.moe_router_topk(x, wr, route, lg, stream))
+    ms_layer = timed(lambda: moeq4.moe_layer_router(x, wr, W, route, y, ws, lg, stream))
+    if moeq4.moe_get_device_error(route) != 0:
+        raise RuntimeError("device error word set in the router run")
+    pk, _ = peaks()
+    flops = 2.0 * T * E * d
+    nbytes = T * d * 2 + E * d * 2 + T * E * 4 + T * k * 8
+    t = ms_router * 1e-3
+    bound = "tensor" if flops / (pk["bf16_tflops"] * 1e12) >= nbytes / (pk["hbm_gbs"] * 1e9) else "hbm"
+    roof = {"bound": bound, "achieved_tflops": flops / t / 1e12, "achieved_gbs": nbytes / t / 1e9,
+            "frac": max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)) / t,
+            "kernel": "router_topk_kernel (projection + top-k)"}
+    return {"T": T, "value": T / t, "unit": UNIT, "ms_per_step": ms_router, "roofline": roof,
+            "l2": "flushed (256 MB write) before every timed call",
+            "layer_from_hidden_states": {"value": T / (ms_layer * 1e-3), "unit": UNIT,
+                                         "ms_per_step": ms_layer},
+            "launches": 5 * steps}
+
+
 def run_ours(args):
     from routing_q4_grouped_gb300 import synth
 
@@ -554,6 +609,9 @@ def run_ours(args):
                                              "roofline", "layer_roofline", "grouped_gemm",
                                              "touched_experts", "e2e", "clocks")}
             wl[name]["unit"] = UNIT
+        rt = measure_router(args.workload, args.steps, args.warmup)
+        launches += rt.pop("launches")
+        wl["router_" + args.workload] = rt
         line["workloads"] = wl
     line["gpu_launches"] = launches
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -194,6 +194,36 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  *  - it calls no cudaMalloc, cudaFree or allocating library routine. */
 moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void* stream);
 
+/* Router projection with the top-k selection fused into its epilogue ([C] "Qwen
+ * 구조와 Prefill 경로": the router picks 8 of 256 experts per token; "GPU 상주와 메모리
+ * 절감": per-token expert selection stays on the GPU):
+ *   logits[t][e] = sum_c x[t][c] * Wr[e][c]   (bf16 inputs, fp32 accumulation)
+ *   out->ids[t][j] = the k largest logits of token t, descending, ties to the lower index
+ *   out->w[t][j]   = exp(l_j - l_max) / sum over the chosen of exp(l - l_max), fp64 -> fp32
+ *   x         bf16 [T][d] token activations (device)
+ *   w_router  bf16 [E][d] router weights, E = out->E (device)
+ *   logits    fp32 [T][E] (device) or NULL when only the choice is wanted
+ *   out       only ids, w and err are written; T, E, k describe them
+ * Limits: E % 16 == 0, E <= 256, k <= 8, d % 64 == 0. Non-finite logits rank as
+ * -inf and set MOE_DEVERR_NONFINITE_LOGIT. One kernel launch (tcgen05, 128 tokens
+ * per CTA). T = 0 launches nothing. */
+moe_status moe_router_topk(const uint16_t* x, const uint16_t* w_router, int32_t T, int32_t d,
+                           float* logits, const moe_route_out* out, void* stream);
+
+/* The rest of the routing (histogram, prefix scan, scatter, block map, as in
+ * moe_route) from chosen experts already in out->ids and out->w, e.g. written
+ * by moe_router_topk. An id outside [0, E) sets MOE_DEVERR_BAD_TILE and counts
+ * as expert 0. ws as for moe_route. */
+moe_status moe_route_ids(const moe_route_out* out, void* ws, size_t ws_bytes, void* stream);
+
+/* The layer from hidden states: moe_router_topk, moe_route_ids and
+ * moe_expert_ffn on one stream, no host sync. logits may be NULL; ws of
+ * moe_layer_workspace_size(...) bytes, zero-filled before first use. The
+ * router limits above apply. */
+moe_status moe_layer_router(const uint16_t* x, const uint16_t* w_router, int32_t T,
+                            const moe_q4_packed* W, float* logits, const moe_route_out* r,
+                            uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+
 /* Grouped expert FFN with in-kernel 4-bit dequantisation ([A] §5-1: weights stay
  * packed, dequantised tile by tile on chip, FP32 accumulation; [C] "Qwen 구조와
  * Prefill 경로"):

@@ -44,7 +44,8 @@ moe_status moe_debug_tmem_layout(uint32_t* out, void* stream);
  * moe_layer record events[i] (cudaEvent_t handles created by the caller) on
  * the call's stream at stage boundaries: 0 before routing, 1 and 2 after the
  * routing kernel, 3 after the gate/up pass, 4 and 5 after the down pass (which
- * also writes the bf16 output). n = 0 turns it off. Process-wide;
+ * also writes the bf16 output), 6 and 7 before and after the fused router
+ * (moe_router_topk). n = 0 turns it off. Process-wide;
  * not for concurrent use from several threads. */
 moe_status moe_debug_set_stage_events(void* const* events, int32_t n);
 

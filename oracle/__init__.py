@@ -203,6 +203,19 @@ def route(logits, k: int, block_m: int = 128) -> Route:
     return Route(T, E, k, block_m, ids, w, counts, offsets.astype(np.int32), perm, inv, tiles)
 
 
+def router_logits(x_bits, wr_bits) -> np.ndarray:
+    """Router projection: logits[t, e] = sum_c x[t, c] * Wr[e, c].
+
+    The router scores every expert for every token before the top-k choice
+    ([C] "Qwen 구조와 Prefill 경로": 8 of 256 experts per token; "GPU 상주와 메모리
+    절감": the selection stays on the GPU). x [T, d] and Wr [E, d] are bf16 bits;
+    products of bf16 values accumulate in float64. Returns float64 [T, E].
+    """
+    X = bf16_value(np.asarray(x_bits))
+    Wr = bf16_value(np.asarray(wr_bits))
+    return X @ Wr.T
+
+
 # ---------------------------------------------------------------------------- FFN
 
 

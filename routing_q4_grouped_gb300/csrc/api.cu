@@ -161,16 +161,19 @@ RouteArgs make_route_args(const float* logits, const moe_route_out* r, void* ws)
   return a;
 }
 
+// ids_given: the chosen experts and weights are already in r->ids / r->w (the
+// fused router wrote them); logits are then not read.
 moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, size_t ws_bytes,
-                      cudaStream_t s) {
+                      cudaStream_t s, int ids_given = 0) {
   moe_status st = check_route_out(r);
   if (st != MOE_OK) return st;
-  if ((!logits && r->T > 0) || !ws) return MOE_ERR_ARG;
+  if ((!ids_given && !logits && r->T > 0) || !ws) return MOE_ERR_ARG;
   if (!aligned16(logits) || !aligned16(ws)) return MOE_ERR_ALIGN;
   if (ws_bytes < route_ws_layout(r->T, r->E, r->k).total) return MOE_ERR_WORKSPACE;
   DevInfo di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const RouteArgs a = make_route_args(logits, r, ws);
+  RouteArgs a = make_route_args(logits, r, ws);
+  a.ids_given = ids_given;
   stage_mark(0, s);
   if (launch_route(a, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
   stage_mark(1, s);
@@ -221,6 +224,7 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
   a.gbar = reinterpret_cast<int32_t*>(base + L.ctr);
   a.err = r->err;
   a.timeout_ns = timeout_ns();
+  a.prefetch_guess = static_cast<long long>(T) * k <= 32ll * E;
   const int n_sh_tiles = fs ? (T + tile_rows - 1) / tile_rows : 0;
 
   const CUtensorMapSwizzle SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -271,6 +275,43 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// defer_weights: leave the chosen logits in r->w for the routing kernel (mode 2)
+moe_status router_impl(const uint16_t* x, const uint16_t* w_router, int32_t T, int32_t d,
+                       float* logits, const moe_route_out* r, cudaStream_t s,
+                       bool defer_weights = false) {
+  moe_status st = check_route_out(r);
+  if (st != MOE_OK) return st;
+  if (T != r->T) return MOE_ERR_SHAPE;
+  if (r->E % 16 || r->E > kRouterMaxE || r->k > kRouterMaxK) return MOE_ERR_SHAPE;
+  if (d < 64 || d % 64 || d > 16384) return MOE_ERR_SHAPE;
+  if (T > 0 && (!x || !w_router)) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return MOE_ERR_ALIGN;
+  DevInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  CUtensorMap mx, mw;
+  const CUtensorMapSwizzle SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_2d(&mx, BF16, 2, x, d, T, 64, 128, SW128) ||
+      !encode_2d(&mw, BF16, 2, w_router, d, r->E, 64, r->E, SW128))
+    return MOE_ERR_CUDA;
+  RouterArgs a{};
+  a.T = T;
+  a.d = d;
+  a.E = r->E;
+  a.k = r->k;
+  a.logits = logits;
+  a.ids = r->ids;
+  a.w = r->w;
+  a.err = r->err;
+  a.timeout_ns = timeout_ns();
+  a.defer_weights = defer_weights ? 1 : 0;
+  stage_mark(6, s);
+  if (launch_router(a, mx, mw, s) != cudaSuccess) return MOE_ERR_CUDA;
+  stage_mark(7, s);
+  return MOE_OK;
+}
 
 // ---- fixed scratch for moe_route_noalloc (no counterpart on the pages)
 constexpr int kNoAllocMaxT = 8192;
@@ -409,6 +450,36 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
   if (W->E != r->E) return MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = route_impl(logits, r, ws, rsz, s)) != MOE_OK) return st;
+  return ffn_impl(x, T, W->d, W, r, y, static_cast<char*>(ws) + rsz, ws_bytes - rsz, s);
+}
+
+moe_status moe_router_topk(const uint16_t* x, const uint16_t* w_router, int32_t T, int32_t d,
+                           float* logits, const moe_route_out* out, void* stream) {
+  return router_impl(x, w_router, T, d, logits, out, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route_ids(const moe_route_out* out, void* ws, size_t ws_bytes, void* stream) {
+  return route_impl(nullptr, out, ws, ws_bytes, static_cast<cudaStream_t>(stream), 1);
+}
+
+moe_status moe_layer_router(const uint16_t* x, const uint16_t* w_router, int32_t T,
+                            const moe_q4_packed* W, float* logits, const moe_route_out* r,
+                            uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!W || !r) return MOE_ERR_ARG;
+  if (r->T != T) return MOE_ERR_SHAPE;
+  const size_t need = moe_layer_workspace_size(T, r->E, r->k, W->d, W->f, W->f_s, r->block_m);
+  if (!ws || need == 0 || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  const size_t rsz = align256(moe_route_workspace_size(T, r->E, r->k));
+  moe_status st;
+  // validate everything before anything is enqueued
+  if ((st = check_packed(W)) != MOE_OK) return st;
+  if ((st = check_route_out(r)) != MOE_OK) return st;
+  if (T > 0 && (!x || !y)) return MOE_ERR_ARG;
+  if (W->E != r->E) return MOE_ERR_SHAPE;
+  if (r->E % 16 || r->E > kRouterMaxE || r->k > kRouterMaxK) return MOE_ERR_SHAPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = router_impl(x, w_router, T, W->d, logits, r, s, true)) != MOE_OK) return st;
+  if ((st = route_impl(nullptr, r, ws, rsz, s, 2)) != MOE_OK) return st;
   return ffn_impl(x, T, W->d, W, r, y, static_cast<char*>(ws) + rsz, ws_bytes - rsz, s);
 }
 

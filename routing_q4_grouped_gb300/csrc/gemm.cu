@@ -381,6 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // With short expert groups nearly every expert is touched and routed tile ti
+  // is expert ti's, so the weights of this CTA's first units are known before
+  // the block map is: start them towards L2 while the previous kernel on the
+  // stream (the routing) still runs. A wrong guess only costs an idle
+  // memory system some bandwidth.
+  if (a.prefetch_guess && warp == kProdWarp0 && lane == 0) {
+    for (int i = 0; i < 2; ++i) {
+      const int u = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+      const int ti = u / a.n_fb;
+      if (ti < a.E) {
+        Unit G{};
+        G.e = ti;
+        G.p = u - ti * a.n_fb;
+        G.K = a.K;
+        G.shared = false;
+        prefetch_unit(a, G);
+      }
+    }
+  }
   // The prologue above may overlap the previous kernel on the stream; from here
   // on its outputs are read (block map, token rows) and written (y_acc).
   griddep_wait();

@@ -41,6 +41,9 @@ struct RouteArgs {
   uint64_t* lb;             // [nblk][E] lookback words (epoch | status | count)
   int32_t* ctr;             // [3] counters
   uint64_t timeout_ns;
+  int ids_given;            // 0: select from logits; 1: ids and w already hold the choice and
+                            // its weights; 2: ids hold the choice and w its logits (descending),
+                            // from which the weights are computed
 };
 
 // Most blocks a call over T tokens can use (blocks of at least kRouteTokensMin tokens).
@@ -77,6 +80,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Optional stage events (bench/test timing): mark(i) records event i on `s`.
 void stage_mark(int i, cudaStream_t s);
+
+// ------------------------------------------------------ router projection
+
+constexpr int kRouterMaxE = 256;           // experts (MMA N) of the fused router at most
+constexpr int kRouterMaxK = 8;             // top-k of the fused router at most
+
+struct RouterArgs {
+  int T, d, E, k;
+  float* logits;            // [T][E] fp32 output, or nullptr
+  int32_t* ids;             // [T][k] chosen experts, descending logit, ties to the lower index
+  float* w;                 // [T][k] renormalised softmax weights (or the chosen logits)
+  int32_t* err;
+  uint64_t timeout_ns;
+  int defer_weights;        // write the chosen logits into w and leave the weights to the
+                            // routing kernel (which spreads the fp64 work over more SMs)
+};
+// TMA maps: x [T][d] bf16 (box 64 x 128), router weights [E][d] bf16 (box 64 x E).
+cudaError_t launch_router(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                          cudaStream_t s);
+size_t router_smem_bytes();
 
 // ------------------------------------------------- kernel-native weight layout
 //
@@ -142,6 +165,8 @@ struct GemmArgs {
   int32_t* gbar;            // pass 1: [2] barrier arrivals and departures (zero between calls)
   int32_t* err;
   uint64_t timeout_ns;
+  int prefetch_guess;       // prefetch the weights of tile ti = expert ti before the block map
+                            // is known (short expert groups: nearly every expert touched)
 };
 
 // TMA descriptors of one pass: token rows B (routed, shared) and the activation

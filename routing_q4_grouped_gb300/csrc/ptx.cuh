@@ -273,6 +273,18 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// mma_ss issued by one elected lane of a converged warp (warp-uniform operands).
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // One K-chunk of two A tiles (4 K-steps of 16 each, 8 MMAs) issued by one elected
 // lane of a converged warp: D tile j at d_j, A tile j at a + 32 j + 8 kk (TMEM
 // columns), B at b + 2 kk (smem descriptor, 32-byte K steps). The first K step

@@ -233,11 +233,38 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
   const int P = 32 / kp;
   constexpr int kPackMax = 4;         // rows held in registers at a time (P may be larger)
-  for (int pk = warp; pk * P < nt; pk += kRouteWarps) {
+  if (a.ids_given == 1) {
+    // the chosen experts and their weights were written by the fused router:
+    // read the experts; an id out of range is reported and counted as expert 0
+    // so that the permutation stays complete
+    for (int i = tid; i < nt * k; i += kRouteThreads) {
+      int e = a.ids[static_cast<size_t>(t0) * k + i];
+      if (e < 0 || e >= E) {
+        atomicOr(a.err, MOE_DEVERR_BAD_TILE);
+        e = 0;
+      }
+      sE[i] = e;
+    }
+  }
+  for (int pk = a.ids_given == 1 ? nt : warp; pk * P < nt; pk += kRouteWarps) {
     const int r0 = pk * P;
     float pv = -INFINITY;             // this lane's packed choice (token lane / kp, rank lane % kp)
     int pe = 0;
-    for (int sb = 0; sb < P && r0 + sb < nt; sb += kPackMax) {
+    if (a.ids_given == 2) {
+      // the fused router chose the experts and left their logits (descending)
+      // in w: only the weights below remain to be computed
+      const int sp = lane / kp, j = lane % kp, i = r0 + sp;
+      if (j < k && i < nt) {
+        const size_t o = static_cast<size_t>(t0 + i) * k + j;
+        pv = a.w[o];
+        pe = a.ids[o];
+        if (pe < 0 || pe >= E) {
+          atomicOr(a.err, MOE_DEVERR_BAD_TILE);
+          pe = 0;
+        }
+      }
+    }
+    for (int sb = 0; a.ids_given == 0 && sb < P && r0 + sb < nt; sb += kPackMax) {
       auto row_ok = [&](int q) { return sb + q < P && r0 + sb + q < nt; };
       uint32_t k0[S], k1[S], k2[S], k3[S];   // keys of the rows, 0 = not a candidate
       {

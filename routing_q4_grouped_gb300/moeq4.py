@@ -71,6 +71,11 @@ _SIGS = {
                                 ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "moe_layer": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4PackedC),
                            ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "moe_router_topk": (_c_i32, [_c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr,
+                                 ctypes.POINTER(RouteOutC), _c_ptr]),
+    "moe_route_ids": (_c_i32, [ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
+    "moe_layer_router": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4PackedC), _c_ptr,
+                                  ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "moe_get_device_error": (_c_i32, [_c_ptr, ctypes.POINTER(_c_i32), _c_ptr]),
     "moe_status_string": (ctypes.c_char_p, [_c_i32]),
     "moe_residual_rms": (_c_i32, [_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr]),
@@ -274,6 +279,37 @@ def moe_layer(x: torch.Tensor, logits: torch.Tensor, W: DeviceWeights, r: RouteB
     wc, rc = W.cstruct(), r.cstruct()
     _check("moe_layer", lib().moe_layer(_ptr(x), _ptr(logits), T, ctypes.byref(wc), ctypes.byref(rc),
                                         _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_router_topk(x: torch.Tensor, w_router: torch.Tensor, out: RouteBuffers,
+                    logits: torch.Tensor = None, stream=None) -> None:
+    """Router projection x [T, d] . w_router [E, d]^T with the top-k fused:
+    writes out.ids / out.w (and logits [T, E] fp32 when given)."""
+    assert x.dtype == torch.bfloat16 and w_router.dtype == torch.bfloat16
+    assert x.is_contiguous() and w_router.is_contiguous()
+    T, d = x.shape
+    rc = out.cstruct()
+    _check("moe_router_topk", lib().moe_router_topk(_ptr(x), _ptr(w_router), T, d, _ptr(logits),
+                                                    ctypes.byref(rc), _stream(stream)))
+
+
+def moe_route_ids(out: RouteBuffers, ws: torch.Tensor, stream=None) -> None:
+    """Histogram, scan, scatter and block map from out.ids / out.w."""
+    rc = out.cstruct()
+    _check("moe_route_ids", lib().moe_route_ids(ctypes.byref(rc), _ptr(ws), ws.numel(),
+                                                _stream(stream)))
+
+
+def moe_layer_router(x: torch.Tensor, w_router: torch.Tensor, W: DeviceWeights, r: RouteBuffers,
+                     y: torch.Tensor, ws: torch.Tensor, logits: torch.Tensor = None,
+                     stream=None) -> None:
+    """The layer from hidden states: fused router, routing from its choice, expert FFN."""
+    assert x.dtype == torch.bfloat16 and w_router.dtype == torch.bfloat16
+    T = x.shape[0]
+    wc, rc = W.cstruct(), r.cstruct()
+    _check("moe_layer_router", lib().moe_layer_router(_ptr(x), _ptr(w_router), T, ctypes.byref(wc),
+                                                      _ptr(logits), ctypes.byref(rc), _ptr(y),
+                                                      _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_residual_rms(y: torch.Tensor, x: torch.Tensor, out: torch.Tensor, stream=None) -> None:

@@ -43,6 +43,7 @@ TID = {
     "dn_qw": 13, "dn_scale": 14, "dn_bias": 15,
     "sgu_qw": 20, "sgu_scale": 21, "sgu_bias": 22,
     "sdn_qw": 23, "sdn_scale": 24, "sdn_bias": 25,
+    "router": 30,
 }
 
 
@@ -143,6 +144,13 @@ def gen_logits(cfg: Config, layer: int = 0, T: int | None = None, t0: int = 0) -
         rank[perm] = np.arange(1, E + 1, dtype=np.float64)
         z = z + 3.0 * (-np.log(rank))[None, :]
     return z.astype(np.float32)
+
+
+def gen_router(cfg: Config, layer: int = 0) -> np.ndarray:
+    """Router weights, bf16 bits [E, d] ~ N(0, 1/d): with x ~ N(0, 1) the logits
+    x . Wr[e] are about N(0, 1), the spread the workloads' logits have."""
+    d, E = cfg.d, cfg.E
+    return to_bf16_bits(normal(cfg.seed, TID["router"], layer, E * d).reshape(E, d) / math.sqrt(d))
 
 
 def _q4_matrix(seed, layer, prefix, experts, rows, K):

@@ -156,3 +156,51 @@ def test_single_expert_and_single_token():
     r = O.route(np.array([[0.3]], np.float32), 1, 128)
     assert r.ids.tolist() == [[0]] and r.w.tolist() == [[1.0]]
     assert r.tiles.tolist() == [[0, 0, 1]]
+
+
+# ------------------------------------------------------------ router projection
+
+
+def test_router_logits_one_hot_rows_pick_columns():
+    # Wr[e] = unit vector at column c_e: the logit is that column of x, exactly
+    cfg = synth.CONFIGS["tiny"]
+    x = synth.gen_x(cfg, 16)
+    cols = np.array([3, 0, 255, 17, 17, 100, 1, 64])
+    wr = np.zeros((8, cfg.d), np.uint16)
+    wr[np.arange(8), cols] = 0x3F80                      # bf16 1.0
+    got = O.router_logits(x, wr)
+    assert np.array_equal(got, O.bf16_value(x)[:, cols])
+
+
+def test_router_logits_constant_rows_are_scaled_row_sums():
+    import math
+    cfg = synth.CONFIGS["tiny"]
+    x = synth.gen_x(cfg, 12)
+    consts = [0.5, -2.0, 0.0078125, 3.0]
+    wr = np.stack([np.full(cfg.d, O.to_bf16(c), np.uint16) for c in consts])
+    got = O.router_logits(x, wr)
+    xv = O.bf16_value(x)
+    for t in range(12):
+        s = math.fsum(float(v) for v in xv[t])
+        for e, c in enumerate(consts):
+            assert abs(got[t, e] - c * s) <= 1e-12 * max(1.0, abs(c * s))
+
+
+def test_router_logits_brute_force_loops():
+    rng = np.random.default_rng(4)
+    x = O.to_bf16(rng.standard_normal((3, 8)))
+    wr = O.to_bf16(rng.standard_normal((4, 8)))
+    xv, wv = O.bf16_value(x), O.bf16_value(wr)
+    got = O.router_logits(x, wr)
+    for t in range(3):
+        for e in range(4):
+            acc = 0.0
+            for c in range(8):
+                acc += float(xv[t, c]) * float(wv[e, c])
+            assert abs(got[t, e] - acc) <= 1e-12
+
+
+def test_router_weights_give_unit_scale_logits():
+    cfg = synth.CONFIGS["t512"]
+    lg = O.router_logits(synth.gen_x(cfg, 256), synth.gen_router(cfg))
+    assert 0.9 < lg.std() < 1.1 and abs(lg.mean()) < 0.05
