@@ -571,6 +571,86 @@ def measure_router(name, steps, warmup):
             "launches": 5 * steps}
 
 
+def measure_decode(steps, warmup):
+    """Small batches (decode steps) through the whole layer on the full-width
+    layer (t512's widths and value recipe): T = 1, 8 and 64, each timed as
+    stream launches and as replays of a captured CUDA graph, against the
+    layer's HBM roofline (the touched experts' and the shared expert's 4-bit
+    weights, x, y and the logits at the measured copy bandwidth)."""
+    import dataclasses
+
+    import torch
+
+    from routing_q4_grouped_gb300 import moeq4, synth
+
+    base = synth.CONFIGS["t512"]
+    pk, _ = peaks()
+    sets = [moeq4.DeviceWeights.from_host(synth.gen_weights(base, 100 + l)) for l in range(2)]
+    out = {}
+    launches = 0
+    for T in (1, 8, 64):
+        cfg = dataclasses.replace(base, T=T)
+        bm = moeq4.default_block_m(T, cfg.E, cfg.k)
+        xs = [torch.from_numpy(synth.gen_x(cfg, T, l).view(np.int16)).cuda().view(torch.bfloat16)
+              for l in range(2)]
+        ls = [torch.from_numpy(synth.gen_logits(cfg, l, T)).cuda() for l in range(2)]
+        r = moeq4.RouteBuffers.alloc(T, cfg.E, cfg.k, bm)
+        ws = moeq4.alloc_workspace(moeq4.moe_layer_workspace_size(T, cfg.E, cfg.k, cfg.d, cfg.f,
+                                                                  cfg.f_s, bm))
+        y = torch.empty((T, cfg.d), dtype=torch.bfloat16, device="cuda")
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                moeq4.moe_layer(xs[i % 2], ls[i % 2], sets[i % 2], r, y, ws, stream)
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                moeq4.moe_layer(xs[i % 2], ls[i % 2], sets[i % 2], r, y, ws, stream)
+            e1.record(stream)
+            stream.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            # one graph per layer set, replayed alternately
+            ms_g, g_err = None, None
+            try:
+                graphs = []
+                for l in range(2):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        moeq4.moe_layer(xs[l], ls[l], sets[l], r, y, ws, stream)
+                    graphs.append(g)
+                for i in range(warmup):
+                    graphs[i % 2].replay()
+                stream.synchronize()
+                e0.record(stream)
+                for i in range(steps):
+                    graphs[i % 2].replay()
+                e1.record(stream)
+                stream.synchronize()
+                ms_g = e0.elapsed_time(e1) / steps
+            except Exception as ex:   # capture refused: report it, keep the stream figure
+                g_err = f"{type(ex).__name__}: {ex}"[:200]
+                torch.cuda.synchronize()
+        if moeq4.moe_get_device_error(r) != 0:
+            raise RuntimeError("device error word set in the decode run")
+        touched = int((r.counts.cpu().numpy() > 0).sum())
+        nbytes = layer_bytes(cfg, T, touched)
+        t_roof = nbytes / (pk["hbm_gbs"] * 1e9)
+        out[f"T{T}"] = {
+            "value": T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "graph": ({"value": T / (ms_g * 1e-3), "ms_per_step": ms_g} if ms_g else
+                      {"error": g_err}),
+            "path": "decode kernels" if T <= 2 else "tensor-core grouped GEMM",
+            "touched_experts": touched,
+            "roofline": {"bound": "hbm", "bytes": nbytes, "roofline_us": t_roof * 1e6,
+                         "achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "frac": t_roof / (ms * 1e-3),
+                         "frac_graph": t_roof / (ms_g * 1e-3) if ms_g else None,
+                         "peak_gbs": pk["hbm_gbs"]}}
+        launches += 4 * steps
+    out["launches"] = launches
+    return out
+
+
 def run_ours(args):
     from routing_q4_grouped_gb300 import synth
 
@@ -612,6 +692,9 @@ def run_ours(args):
         rt = measure_router(args.workload, args.steps, args.warmup)
         launches += rt.pop("launches")
         wl["router_" + args.workload] = rt
+        dec = measure_decode(args.steps, args.warmup)
+        launches += dec.pop("launches")
+        wl["decode"] = dec
         line["workloads"] = wl
     line["gpu_launches"] = launches
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

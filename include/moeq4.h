@@ -156,7 +156,10 @@ size_t moe_ffn_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_
                               int32_t f_s, int32_t block_m);
 
 /* Bytes of scratch for moe_layer: the routing part followed by the FFN part.
- * Zero-fill it before first use (the routing part must start zeroed). */
+ * Zero-fill it before first use (the routing part must start zeroed). The
+ * split between the two parts depends on T: a workspace serves calls with the
+ * T it was sized for; for another T use another workspace, or zero-fill it
+ * again before the first call with the new T. */
 size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
                                 int32_t f_s, int32_t block_m);
 
@@ -238,6 +241,18 @@ moe_status moe_layer_router(const uint16_t* x, const uint16_t* w_router, int32_t
 moe_status moe_expert_ffn(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed* W,
                           const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* moe_expert_ffn for small batches (decode steps, short prompts: T <= 64).
+ * With a few tokens per expert the layer streams 4-bit weights ([A] §6:
+ * batch-1 decode is bound by memory bandwidth), so each touched expert's work
+ * is split along K over many CTAs and multiplied on the CUDA cores with fp32
+ * accumulation: three launches (gate/up partial sums, SwiGLU + down with the
+ * weighted combine, bf16 output). Same arguments, result and workspace as
+ * moe_expert_ffn, which takes this path by itself for T <= 2. T > 64 returns
+ * MOE_ERR_SHAPE. */
+moe_status moe_expert_ffn_decode(const uint16_t* x, int32_t T, int32_t d,
+                                 const moe_q4_packed* W, const moe_route_out* r, uint16_t* y,
+                                 void* ws, size_t ws_bytes, void* stream);
 
 /* moe_route followed by moe_expert_ffn on the same stream, no host sync.
  *   x bf16 [T][d], logits fp32 [T][E]; r receives the routing result; y bf16 [T][d].

@@ -49,6 +49,11 @@ moe_status moe_debug_tmem_layout(uint32_t* out, void* stream);
  * not for concurrent use from several threads. */
 moe_status moe_debug_set_stage_events(void* const* events, int32_t n);
 
+/* Largest batch for which moe_expert_ffn (and moe_layer) take the decode
+ * path instead of the tensor-core grouped GEMM; 0 = never. Process-wide; the
+ * default is 2. For tests and measurements. */
+moe_status moe_debug_set_decode_max_t(int32_t t);
+
 /* Device address and size of the fixed scratch array that moe_route_noalloc
  * uses on the current device (looked up with that device current), so that a
  * test can plant stale contents in it. */

@@ -1,5 +1,6 @@
 // api.cu — the extern "C" boundary of libmoeq4: argument validation,
 // workspace layout, TMA descriptor encoding and the launch sequence.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -181,9 +182,14 @@ moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, siz
   return MOE_OK;
 }
 
+// Batches of at most this many tokens take the decode path (split-K CUDA-core
+// kernels); process-wide, changed by moe_debug_set_decode_max_t.
+std::atomic<int> g_decode_max_t{kDecodeAutoT};
+
+// path: 0 = by batch size, 1 = decode kernels, 2 = tensor-core grouped GEMM
 moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed* W,
                     const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
-                    cudaStream_t s) {
+                    cudaStream_t s, int path = 0) {
   moe_status st = check_route_out(r);
   if (st != MOE_OK) return st;
   if ((st = check_packed(W)) != MOE_OK) return st;
@@ -201,6 +207,41 @@ moe_status ffn_impl(const uint16_t* x, int32_t T, int32_t d, const moe_q4_packed
   if (T == 0) return MOE_OK;
 
   char* base = static_cast<char*>(ws);
+  const bool decode_fits = T <= kDecodeMaxT && decode_gu_bytes(T, k, d, f, fs) <= L.act_sh - L.act;
+  if (path == 1 && !decode_fits) return MOE_ERR_SHAPE;
+  if (path == 1 || (path == 0 && decode_fits && T <= g_decode_max_t.load())) {
+    DecodeArgs a{};
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.d = d;
+    a.f = f;
+    a.f_s = fs;
+    a.f_max = f > fs ? f : fs;
+    a.x = x;
+    a.tiles = r->tiles;
+    a.n_tiles = r->n_tiles;
+    a.max_tiles = max_tiles;
+    a.n_sh_tiles = fs ? (T + kDecTileRows - 1) / kDecTileRows : 0;
+    a.perm = r->perm;
+    a.wts = r->w;
+    a.n_fb = P.gu.units;
+    a.n_fb_sh = P.sgu.units;
+    a.n_fb_max = a.n_fb > a.n_fb_sh ? a.n_fb : a.n_fb_sh;
+    a.pk_gu = pk + P.gu.offset;
+    a.pk_gu_sh = pk + P.sgu.offset;
+    a.pk_dn = pk + P.dn.offset;
+    a.pk_dn_sh = pk + P.sdn.offset;
+    a.gu_part = reinterpret_cast<float*>(base + L.act);
+    a.n_slots = T * k + T;
+    a.y_acc = reinterpret_cast<float*>(base + L.y_acc);
+    a.y = y;
+    a.err = r->err;
+    if (launch_decode(a, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    stage_mark(4, s);
+    stage_mark(5, s);
+    return MOE_OK;
+  }
   uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
   uint16_t* act_sh = reinterpret_cast<uint16_t*>(base + L.act_sh);
   const uint64_t act_rows = act_rows_capacity(T, k, max_tiles);
@@ -451,6 +492,18 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = route_impl(logits, r, ws, rsz, s)) != MOE_OK) return st;
   return ffn_impl(x, T, W->d, W, r, y, static_cast<char*>(ws) + rsz, ws_bytes - rsz, s);
+}
+
+moe_status moe_expert_ffn_decode(const uint16_t* x, int32_t T, int32_t d,
+                                 const moe_q4_packed* W, const moe_route_out* r, uint16_t* y,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  return ffn_impl(x, T, d, W, r, y, ws, ws_bytes, static_cast<cudaStream_t>(stream), 1);
+}
+
+moe_status moe_debug_set_decode_max_t(int32_t t) {
+  if (t < 0) return MOE_ERR_ARG;
+  g_decode_max_t.store(t);
+  return MOE_OK;
 }
 
 moe_status moe_router_topk(const uint16_t* x, const uint16_t* w_router, int32_t T, int32_t d,

@@ -853,7 +853,11 @@ FfnWs ffn_ws_layout(int T, int k, int d, int f, int f_s, int max_tiles) {
   w.ctr = o;
   o = 256;
   w.act = o;
-  o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(act_rows_capacity(T, k, max_tiles)) * f, 256);
+  // the activations of the grouped GEMM, or (same region) the gate/up partial
+  // sums of the small-batch path
+  size_t act_bytes = sizeof(uint16_t) * static_cast<size_t>(act_rows_capacity(T, k, max_tiles)) * f;
+  if (T <= kDecodeMaxT) act_bytes = std::max(act_bytes, decode_gu_bytes(T, k, d, f, f_s));
+  o = align_up(o + act_bytes, 256);
   w.act_sh = o;
   o = align_up(o + sizeof(uint16_t) * align_up(static_cast<size_t>(T), kNMax) * f_s, 256);
   w.y_acc = o;

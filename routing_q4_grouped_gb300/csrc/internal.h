@@ -194,6 +194,37 @@ cudaError_t launch_gemm(int mode, int tile_rows, const GemmArgs& a, const GemmMa
 
 
 size_t gemm_smem_bytes();
+
+// ------------------------------------------------------- small-batch expert FFN
+
+constexpr int kDecTileRows = 64;           // token rows per tile at most (decode path)
+constexpr int kDecodeMaxT = 64;            // largest batch the decode path takes
+constexpr int kDecodeAutoT = 2;            // moe_expert_ffn takes it for batches up to this
+                                           // (measured: faster than the grouped GEMM at T <= 2)
+
+struct DecodeArgs {
+  int T, k, E, d, f, f_s, f_max;
+  const uint16_t* x;        // [T][d] bf16
+  const int32_t* tiles;     // routed block map [n][3], tiles of at most kDecTileRows rows
+  const int32_t* n_tiles;   // device count
+  int max_tiles;            // capacity of the block map
+  int n_sh_tiles;           // shared-expert tiles of kDecTileRows tokens
+  const int32_t* perm;
+  const float* wts;
+  int n_fb, n_fb_sh, n_fb_max;   // gate/up units (256 rows) per routed / shared expert, larger
+  const uint8_t* pk_gu;     // packed matrices (kernel-native layout)
+  const uint8_t* pk_gu_sh;
+  const uint8_t* pk_dn;
+  const uint8_t* pk_dn_sh;
+  float* gu_part;           // [gate/up K-slices][n_slots][2 f_max] partial sums
+  int n_slots;              // T*k routed rows + T shared rows
+  float* y_acc;             // [T][d] fp32 combine buffer
+  uint16_t* y;              // [T][d] bf16 output
+  int32_t* err;
+};
+size_t decode_gu_bytes(int T, int k, int d, int f, int f_s);
+// decode_gate_up, decode_down, decode_finalize on stream s (programmatic serialization).
+cudaError_t launch_decode(const DecodeArgs& a, int sms, cudaStream_t s);
 // Max rows per unit and rows per shared-expert tile for a block map of at most
 // block_m rows per tile: 64 when block_m <= 64 (deeper tensor-memory pipeline),
 // else 128.

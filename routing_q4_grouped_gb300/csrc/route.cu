@@ -208,6 +208,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   int* sLead = sOff + E + 1;           // [kRouteThreads] group base handed to peers
 
   griddep_launch_dependents();   // the GEMM that follows may start its prologue
+  // launched with programmatic serialization (a one-block grid): the previous
+  // kernel on the stream may still read the arrays this call rewrites
+  griddep_wait();
   if (tid == 0) {
     s_b = atomicAdd(&a.ctr[kCtrTicket], 1);   // virtual block id = arrival order
     s_epoch = static_cast<uint32_t>(a.ctr[kCtrEpoch]);
@@ -529,6 +532,10 @@ static cudaError_t launch_s(RouteArgs a, int sms, cudaStream_t s) {
     if (per_sm > 0 && nblk <= per_sm * sms) {
       a.tpb = tpb;
       a.nblk = nblk;
+      // one block has no other block to wait for: an ordinary launch, which may
+      // overlap the previous kernel's tail (programmatic serialization)
+      if (nblk == 1)
+        return launch_pdl(route_kernel<S>, dim3(1), dim3(kRouteThreads), smem, s, a);
       void* args[] = {&a};
       return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(route_kernel<S>), nblk,
                                          kRouteThreads, args, smem, s);

@@ -71,6 +71,9 @@ _SIGS = {
                                 ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "moe_layer": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4PackedC),
                            ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "moe_expert_ffn_decode": (_c_i32, [_c_ptr, _c_i32, _c_i32, ctypes.POINTER(Q4PackedC),
+                                       ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "moe_debug_set_decode_max_t": (_c_i32, [_c_i32]),
     "moe_router_topk": (_c_i32, [_c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr,
                                  ctypes.POINTER(RouteOutC), _c_ptr]),
     "moe_route_ids": (_c_i32, [ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
@@ -269,6 +272,23 @@ def moe_expert_ffn(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.
     wc, rc = W.cstruct(), r.cstruct()
     _check("moe_expert_ffn", lib().moe_expert_ffn(_ptr(x), T, d, ctypes.byref(wc), ctypes.byref(rc),
                                                   _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn_decode(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.Tensor,
+                          ws: torch.Tensor, stream=None) -> None:
+    """The small-batch expert FFN (T <= 64): split-K weight streaming on the CUDA cores."""
+    assert x.dtype == torch.bfloat16 and y.dtype == torch.bfloat16
+    assert x.is_contiguous() and y.is_contiguous()
+    T, d = x.shape
+    wc, rc = W.cstruct(), r.cstruct()
+    _check("moe_expert_ffn_decode",
+           lib().moe_expert_ffn_decode(_ptr(x), T, d, ctypes.byref(wc), ctypes.byref(rc), _ptr(y),
+                                       _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_debug_set_decode_max_t(t: int) -> None:
+    """Batches of at most t tokens take the decode path in moe_expert_ffn / moe_layer (0 = never)."""
+    _check("moe_debug_set_decode_max_t", lib().moe_debug_set_decode_max_t(t))
 
 
 def moe_layer(x: torch.Tensor, logits: torch.Tensor, W: DeviceWeights, r: RouteBuffers,
