@@ -70,6 +70,9 @@ def parse_args():
                    help="tile rows of the block map; auto = 64 for short expert groups, else 128")
     p.add_argument("--sets", type=int, default=2, help="independent layer sets cycled per step")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--prefetch-mb", type=int, default=32,
+                   help="chunked run: MB of the next layer's weights prefetched into L2 during "
+                        "each layer's tail (0 = off)")
     p.add_argument("--no-workloads", action="store_true",
                    help="time only --workload (not the other single-layer workloads)")
     return p.parse_args()
@@ -779,12 +782,23 @@ def run_chunked(args):
     xb = [torch.empty((C, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     out = torch.empty((nch, C, d), dtype=torch.bfloat16, device="cuda")
 
+    # the next layer's first gate/up weights head for L2 during this layer's
+    # tail, requested from a side stream so that the request never delays the
+    # main stream's next kernels
+    prefetch_bytes = args.prefetch_mb << 20
+    pf_stream = torch.cuda.Stream()
+    pf_events = [torch.cuda.Event() for _ in range(L)]
+
     def run_chunk(x_in, lg, y_out):
         # layers 0..L-1 of one chunk; the last layer writes the chunk's output
         cur = x_in
         for l in range(L):
             last = l + 1 == L
             moeq4.moe_layer(cur, lg[l], layers[l], route, y_out if last else y, ws, stream)
+            if prefetch_bytes:
+                pf_events[l].record(stream)
+                pf_stream.wait_event(pf_events[l])
+                moeq4.moe_l2_prefetch(layers[(l + 1) % L].packed, prefetch_bytes, pf_stream)
             if not last:
                 nxt = xb[l % 2]
                 moeq4.moe_residual_rms(y, cur, nxt, stream)
@@ -909,6 +923,7 @@ def run_chunked(args):
         "data": "synthetic (seeded torch generator on the device, same value recipe; random-init 4-bit weights)",
         "config": {"workload": args.workload, "T": cfg.T, "chunk": C, "layers": L, "d": d, "E": E,
                    "k": k, "f": f, "f_s": fs, "block_m": args.block_m,
+                   "next_layer_prefetch_mb": args.prefetch_mb,
                    "l2": f"inputs larger than L2: {L} layers of {layers[0].nbytes / 1e6:.0f} MB weights per step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
@@ -919,7 +934,8 @@ def run_chunked(args):
                 "h2d_bytes_per_step": x0.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2},
         "clocks": clk,
-        "gpu_launches": (LAUNCHES_PER_LAYER * L + (L - 1)) * nch * args.steps,
+        "gpu_launches": (LAUNCHES_PER_LAYER * L + (L - 1) + (L if prefetch_bytes else 0))
+                        * nch * args.steps,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -270,6 +270,14 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
 moe_status moe_residual_rms(const uint16_t* y, const uint16_t* x, uint16_t* out, int32_t T,
                             int32_t d, void* stream);
 
+/* Asks the GPU to bring [ptr, ptr + bytes) of device memory into L2 (bulk
+ * prefetch requests, no data returned), as one small kernel on `stream` that
+ * may overlap the tail of the previous kernel (programmatic serialization).
+ * In the bounded-chunk run ([A] §5-2) the caller issues it after layer l's FFN
+ * with the first megabytes of layer l+1's packed weights: the gate/up weights
+ * of the experts that layer's first units read. ptr and bytes 16-byte aligned. */
+moe_status moe_l2_prefetch(const void* ptr, size_t bytes, void* stream);
+
 /* Synchronises `stream`, copies the device error word `err` to *code and
  * returns MOE_ERR_DEVICE if it is non-zero, MOE_OK otherwise. */
 moe_status moe_get_device_error(const int32_t* err, int32_t* code, void* stream);

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moeq4.h"
+#include "internal.h"
+#include "ptx.cuh"
 
 namespace moeq4 {
 namespace {
@@ -57,8 +59,35 @@ __global__ void __launch_bounds__(256) residual_rms_kernel(const uint16_t* __res
   }
 }
 
+// L2 prefetch of [p, p + bytes): each thread requests its 64 KB pieces
+// (cp.async.bulk.prefetch.L2, no data returned). Launched with programmatic
+// serialization it runs on the multiprocessors the previous kernel frees.
+__global__ void __launch_bounds__(128) l2_prefetch_kernel(const uint8_t* p, size_t bytes) {
+  griddep_launch_dependents();
+  constexpr size_t kPiece = 65536;
+  const size_t n = (bytes + kPiece - 1) / kPiece;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t off = i * kPiece;
+    const size_t len = bytes - off < kPiece ? bytes - off : kPiece;
+    bulk_prefetch_l2(p + off, static_cast<uint32_t>(len));
+  }
+}
+
 }  // namespace
 }  // namespace moeq4
+
+extern "C" moe_status moe_l2_prefetch(const void* ptr, size_t bytes, void* stream) {
+  if (!ptr) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) || (bytes & 15u)) return MOE_ERR_ALIGN;
+  if (bytes == 0) return MOE_OK;
+  const size_t pieces = (bytes + 65535) / 65536;
+  const int blocks = static_cast<int>(pieces < 128 * 16 ? (pieces + 127) / 128 : 16);
+  cudaError_t e = moeq4::launch_pdl(moeq4::l2_prefetch_kernel, dim3(blocks), dim3(128), 0,
+                                    static_cast<cudaStream_t>(stream),
+                                    static_cast<const uint8_t*>(ptr), bytes);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 extern "C" moe_status moe_residual_rms(const uint16_t* y, const uint16_t* x, uint16_t* out,
                                        int32_t T, int32_t d, void* stream) {

@@ -79,6 +79,8 @@ _SIGS = {
     "moe_route_ids": (_c_i32, [ctypes.POINTER(RouteOutC), _c_ptr, _c_size, _c_ptr]),
     "moe_layer_router": (_c_i32, [_c_ptr, _c_ptr, _c_i32, ctypes.POINTER(Q4PackedC), _c_ptr,
                                   ctypes.POINTER(RouteOutC), _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "moe_l2_prefetch": (_c_i32, [_c_ptr, _c_size, _c_ptr]),
+
     "moe_get_device_error": (_c_i32, [_c_ptr, ctypes.POINTER(_c_i32), _c_ptr]),
     "moe_status_string": (ctypes.c_char_p, [_c_i32]),
     "moe_residual_rms": (_c_i32, [_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_ptr]),
@@ -337,6 +339,13 @@ def moe_residual_rms(y: torch.Tensor, x: torch.Tensor, out: torch.Tensor, stream
     T, d = x.shape
     _check("moe_residual_rms", lib().moe_residual_rms(_ptr(y), _ptr(x), _ptr(out), T, d,
                                                       _stream(stream)))
+
+
+def moe_l2_prefetch(t: torch.Tensor, nbytes: int = None, stream=None) -> None:
+    """Prefetch the first nbytes (default all) of device tensor t into L2."""
+    n = t.numel() * t.element_size() if nbytes is None else min(nbytes, t.numel() * t.element_size())
+    n -= n % 16
+    _check("moe_l2_prefetch", lib().moe_l2_prefetch(_ptr(t), n, _stream(stream)))
 
 
 def moe_get_device_error(r: RouteBuffers, stream=None) -> int:

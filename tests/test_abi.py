@@ -56,6 +56,29 @@ def test_host_side_sizes(L):
     assert "workspace" in L.status_string(-3)
 
 
+def test_router_and_prefetch_arguments_rejected_on_host(L):
+    lib = L.lib()
+    fake = 1 << 20
+    assert lib.moe_l2_prefetch(None, 16, None) == -1                  # no pointer
+    assert lib.moe_l2_prefetch(fake + 8, 16, None) == -7              # misaligned start
+    assert lib.moe_l2_prefetch(fake, 24, None) == -7                  # length not a multiple of 16
+    assert lib.moe_l2_prefetch(fake, 0, None) == 0                    # nothing to do
+    r = L.RouteOutC()
+    for f in ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "n_tiles", "err"):
+        setattr(r, f, fake)
+    r.T, r.E, r.k, r.block_m = 16, 256, 9, 128                        # k above the router's 8
+    assert lib.moe_router_topk(fake, fake, 16, 2048, fake, ctypes.byref(r), None) == -2
+    r.E, r.k = 250, 8                                                 # E not a multiple of 16
+    assert lib.moe_router_topk(fake, fake, 16, 2048, fake, ctypes.byref(r), None) == -2
+    r.E = 256
+    assert lib.moe_router_topk(fake, fake, 16, 2000, fake, ctypes.byref(r), None) == -2   # d % 64
+    assert lib.moe_router_topk(fake, fake, 15, 2048, fake, ctypes.byref(r), None) == -2   # T mismatch
+    assert lib.moe_router_topk(None, fake, 16, 2048, fake, ctypes.byref(r), None) == -1   # no x
+    assert lib.moe_router_topk(fake, fake, 16, 2048, fake + 4, ctypes.byref(r), None) == -7
+    assert lib.moe_route_ids(ctypes.byref(r), fake, 0, None) == -3   # workspace too small
+    assert lib.moe_debug_set_decode_max_t(-1) == -1
+
+
 def test_bad_arguments_rejected_on_host(L):
     lib = L.lib()
     r = L.RouteOutC()                       # all NULL

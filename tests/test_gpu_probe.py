@@ -146,3 +146,13 @@ def test_prepack_matches_documented_layout():
         _pack_reference(W.sdn_qw, W.sdn_scale, W.sdn_bias, 1, cfg.d)])
     assert got.shape == ref.shape
     assert np.array_equal(got, ref)
+
+
+def test_l2_prefetch_leaves_data_and_errors_alone():
+    t = torch.arange(1 << 20, dtype=torch.int32, device="cuda")
+    before = t.clone()
+    moeq4.moe_l2_prefetch(t)
+    moeq4.moe_l2_prefetch(t, 4096 + 16)
+    torch.cuda.synchronize()
+    assert torch.equal(t, before)
+    assert moeq4.lib().moe_l2_prefetch(None, 16, None) == -1            # MOE_ERR_ARG
