@@ -49,7 +49,7 @@ typedef int32_t moe_status;
 
 /* Bits of the device error word. */
 #define MOE_DEVERR_NONFINITE_LOGIT  1  /* a router logit was NaN/Inf (treated as -inf) */
-#define MOE_DEVERR_SCAN_TIMEOUT     2  /* decoupled-lookback wait gave up */
+#define MOE_DEVERR_SCAN_TIMEOUT     2  /* reserved (routing has no waits; never set) */
 #define MOE_DEVERR_PIPE_TIMEOUT     4  /* a GEMM pipeline or grid barrier wait gave up */
 #define MOE_DEVERR_BAD_TILE         8  /* a block-map entry was out of range */
 #define MOE_DEVERR_BAD_WORKSPACE   16  /* routing or FFN scratch counters were not zero at
@@ -138,14 +138,10 @@ typedef struct moe_route_out {
 /* Upper bound on the block-map length: T*k/block_m + min(E, T*k). */
 int32_t moe_route_max_tiles(int32_t T, int32_t E, int32_t k, int32_t block_m);
 
-/* Bytes of scratch for moe_route: 256 bytes of counters (block ticket, blocks
- * done, call epoch), then the epoch-tagged lookback words of the prefix scan.
- * Zero-fill the buffer before its first use. A call that completes leaves the
- * ticket and done counters at zero again but advances the epoch and leaves
- * its lookback words behind (the next call's epoch makes them stale): keep the
- * buffer untouched between routing calls, and do not reuse it for anything
- * that expects zeroed memory. After a call that set a device error bit,
- * zero-fill the whole buffer again before the next call. */
+/* Bytes of scratch for moe_route: one row of per-expert counts per routing
+ * block. Its contents at launch do not matter (every call writes each row
+ * before it reads it) and it needs no zero-filling; calls that overlap on the
+ * GPU must not share it. */
 size_t moe_route_workspace_size(int32_t T, int32_t E, int32_t k);
 
 /* Bytes of scratch for moe_expert_ffn: two grid-barrier counters (256 bytes),
@@ -156,9 +152,9 @@ size_t moe_ffn_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_
                               int32_t f_s, int32_t block_m);
 
 /* Bytes of scratch for moe_layer: the routing part followed by the FFN part.
- * Zero-fill it before first use (the routing part must start zeroed). The
- * split between the two parts depends on T: a workspace serves calls with the
- * T it was sized for; for another T use another workspace, or zero-fill it
+ * Zero-fill it before first use (the FFN part's counters must start zeroed).
+ * The split between the two parts depends on T: a workspace serves calls with
+ * the T it was sized for; for another T use another workspace, or zero-fill it
  * again before the first call with the new T. */
 size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int32_t f,
                                 int32_t f_s, int32_t block_m);
@@ -171,10 +167,11 @@ size_t moe_layer_workspace_size(int32_t T, int32_t E, int32_t k, int32_t d, int3
  *   out     result arrays and T, E, k, block_m (host struct, device arrays)
  *   ws      scratch of moe_route_workspace_size(T, E, k) bytes
  * T = 0 is allowed (counts/offsets zeroed, n_tiles = 0; logits, ids, w, perm
- * and inv may then be NULL). The step is one cooperative kernel launch (its
- * blocks meet at a grid barrier, so the device must hold all of them at once;
- * the block size grows with T to keep the grid resident); a launch the device
- * refuses returns MOE_ERR_CUDA. */
+ * and inv may then be NULL). A batch of at most 8 tokens takes one kernel
+ * launch, a larger one two (choose and count, then place), each launched with
+ * programmatic stream serialization; no block waits on another, and inv holds
+ * the rows' local ranks between the two. A launch the device refuses returns
+ * MOE_ERR_CUDA. */
 moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, size_t ws_bytes,
                      void* stream);
 
@@ -183,15 +180,14 @@ moe_status moe_route(const float* logits, const moe_route_out* out, void* ws, si
  * such as a serving process that reserves all device memory up front and hands
  * out fixed arenas, or a plugin that has no access to its host framework's
  * allocator. Same inputs, outputs and results as moe_route, but its scratch is
- * a fixed array inside the library (about 2 MB, held on every GPU that loads
- * the library until the process exits), so:
+ * a fixed array inside the library (1 MB, held on every GPU that loads the
+ * library until the process exits), so:
  *  - sizes are limited to T <= 8192, E <= 256, k <= 8; larger ones return
  *    MOE_ERR_TOO_LARGE and enqueue nothing;
  *  - the first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture;
- *  - every call shares the one array: each call first clears the counters
- *    that must start at zero and takes a new epoch, so that whatever an
- *    earlier call left behind (even one that did not finish) is ignored; calls
+ *  - every call shares the one array: whatever an earlier call left in it
+ *    (even one that did not finish) is overwritten before it is read; calls
  *    whose work overlaps on the GPU (other streams, other host threads) race
  *    and must be serialised by the caller;
  *  - it calls no cudaMalloc, cudaFree or allocating library routine. */

@@ -156,8 +156,8 @@ RouteArgs make_route_args(const float* logits, const moe_route_out* r, void* ws)
   a.tiles = r->tiles;
   a.n_tiles = r->n_tiles;
   a.err = r->err;
-  a.lb = reinterpret_cast<uint64_t*>(base + L.lb);
-  a.ctr = reinterpret_cast<int32_t*>(base + L.ctr);
+  a.rows = reinterpret_cast<uint32_t*>(base + L.rows);
+  a.max_tiles = moe_route_max_tiles(r->T, r->E, r->k, r->block_m);
   a.timeout_ns = timeout_ns();
   return a;
 }
@@ -176,7 +176,7 @@ moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, siz
   RouteArgs a = make_route_args(logits, r, ws);
   a.ids_given = ids_given;
   stage_mark(0, s);
-  if (launch_route(a, di.sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   stage_mark(1, s);
   stage_mark(2, s);   // (one routing kernel: stages 1 and 2 coincide)
   return MOE_OK;
@@ -358,9 +358,9 @@ moe_status router_impl(const uint16_t* x, const uint16_t* w_router, int32_t T, i
 constexpr int kNoAllocMaxT = 8192;
 constexpr int kNoAllocMaxE = 256;
 constexpr int kNoAllocMaxK = 8;
-// routing scratch at the limits: counters (256 bytes) and the 8-byte lookback
-// words of 1024 blocks (8192 tokens in blocks of at least 8) x 256 experts
-constexpr size_t kNoAllocBytes = 256 + 8 * 1024 * 256;
+// routing scratch at the limits: the 4-byte count rows of 1024 blocks (8192
+// tokens in blocks of at least 8) x 256 experts
+constexpr size_t kNoAllocBytes = 4 * 1024 * 256;
 __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
 // Device address of g_route_scratch on the current device, looked up once per
@@ -378,16 +378,6 @@ moe_status noalloc_scratch(void** out) {
   }
   *out = addr[dev];
   return MOE_OK;
-}
-
-// Opens the fixed scratch for a new call: the ticket and leave counters back to
-// zero and a fresh epoch, so that lookback words left behind by an earlier call
-// that did not finish (its blocks refused out-of-range tickets, for example after
-// two calls overlapped) carry an older epoch and read as unpublished.
-__global__ void noalloc_open_kernel(int32_t* ctr) {
-  ctr[kCtrTicket] = 0;
-  ctr[kCtrLeave] = 0;
-  ctr[kCtrEpoch] = static_cast<int32_t>(static_cast<uint32_t>(ctr[kCtrEpoch]) + 1u);
 }
 
 std::mutex g_ev_mu;
@@ -572,12 +562,8 @@ moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void
   if (L.total > kNoAllocBytes) return MOE_ERR_TOO_LARGE;
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws)) != MOE_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the ticket and leave counters must start at zero and the call needs an epoch
-  // of its own; the lookback words may hold anything
-  noalloc_open_kernel<<<1, 1, 0, s>>>(static_cast<int32_t*>(ws));
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  return route_impl(logits, out, ws, kNoAllocBytes, s);
+  // the count rows may hold anything: each call writes every row it reads
+  return route_impl(logits, out, ws, kNoAllocBytes, static_cast<cudaStream_t>(stream));
 }
 
 const char* moe_status_string(moe_status s) {

@@ -15,19 +15,16 @@ namespace moeq4 {
 
 constexpr int kRouteThreads = 256;         // threads per routing block (8 warps)
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kRouteTokensMin = 8;         // tokens per block at least (2 warps select when k <= 8)
-constexpr int kRouteBlocksTarget = 128;    // blocks per call aimed at (longer lookback chains
-                                           // beyond), fewer tokens per block when T is small
-// Routing counters at the start of the workspace.
-constexpr int kCtrTicket = 0;              // block arrival order = block id (zero between calls)
-constexpr int kCtrLeave = 1;               // blocks done (zero between calls)
-constexpr int kCtrEpoch = 2;               // call number: tags this call's lookback words
+constexpr int kRouteTokensMin = 8;         // tokens per block at least (one per warp)
+constexpr int kRouteBlocksTarget = 128;    // blocks per call aimed at: every placing block reads
+                                           // every block's count row
 
 struct RouteArgs {
   const float* logits;
   int T, E, k, block_m;
   int tpb;                  // tokens per block (set at launch)
   int nblk;                 // blocks = max(1, ceil(T / tpb)) (set at launch)
+  int max_tiles;            // capacity of the block map
   int32_t* ids;
   float* w;
   int32_t* counts;
@@ -38,8 +35,7 @@ struct RouteArgs {
   int32_t* n_tiles;
   int32_t* err;
   // scratch
-  uint64_t* lb;             // [nblk][E] lookback words (epoch | status | count)
-  int32_t* ctr;             // [3] counters
+  uint32_t* rows;           // [nblk][round_up(E, 4)] per-block expert counts
   uint64_t timeout_ns;
   int ids_given;            // 0: select from logits; 1: ids and w already hold the choice and
                             // its weights; 2: ids hold the choice and w its logits (descending),
@@ -52,12 +48,13 @@ inline int route_max_blocks(int T) {
 }
 
 struct RouteWs {
-  size_t ctr, lb, total;
+  size_t rows, total;
 };
 RouteWs route_ws_layout(int T, int E, int k);
 
-// The whole routing step: one cooperative launch (sms = multiprocessors).
-cudaError_t launch_route(const RouteArgs& a, int sms, cudaStream_t s);
+// The whole routing step: one launch for a batch that one block covers, else
+// two (choose and count, then place), each with programmatic serialization.
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel on `s` finishes (it calls griddep_wait before

@@ -1,10 +1,11 @@
-// route.cu — GPU routing for the MoE expert layer in one cooperative kernel:
-// per-token top-k expert selection with renormalised softmax weights, a
-// deterministic per-block histogram with stable local ranks, a single-pass
-// decoupled-lookback prefix over blocks, then (once the last block's inclusive
-// prefixes, the expert totals, are out) the expert offsets, the scatter of
-// rows into their groups and the block map. One launch on one stream, no host
-// synchronisation.
+// route.cu — GPU routing for the MoE expert layer: per-token top-k expert
+// selection with renormalised softmax weights, a deterministic per-block
+// histogram with stable local ranks, every block's prefix over the earlier
+// blocks' counts and the expert totals, the expert offsets, the scatter of rows
+// into their groups and the block map. A batch that one block covers takes one
+// launch; a larger one two (choose and count, then place), chained by
+// programmatic dependent launch on one stream, with no host synchronisation and
+// no block waiting on another.
 //
 // Step order: "Apple silicon용 Lily, Qwen 추론 최적화" (aitrends.kr), section
 // "GPU 상주와 메모리 절감" — per-token expert selection, a histogram of
@@ -13,7 +14,6 @@
 // §5-2 — histogram, prefix scan, scatter and block map in one GPU command buffer.
 #include <cmath>
 #include <climits>
-#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -25,24 +25,6 @@ namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-// Lookback words: [epoch 32 | status 2 | count 30]. A word whose epoch is not
-// the current call's reads as "not published", so the words never need clearing.
-constexpr uint64_t kLbAggregate = 1ull << 30;
-constexpr uint64_t kLbInclusive = 2ull << 30;
-constexpr uint64_t kLbStatus = 3ull << 30;
-constexpr uint32_t kLbValueMask = (1u << 30) - 1;
-
-// Relaxed loads of different words may be in flight together; acquire loads
-// would wait for one another.
-__device__ __forceinline__ uint64_t ld_relaxed64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release64(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // Order-preserving unsigned key of a non-NaN float (larger float, larger key;
 // -inf maps to 0x007FFFFF, so 0 can mark "no candidate").
 __device__ __forceinline__ uint32_t float_key(float x) {
@@ -53,115 +35,149 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Logits of token t held by this lane (experts lane + 32 s); not loaded (left
-// 0) where s is out of range or the token is not loaded.
-template <int S>
-__device__ __forceinline__ void load_row(const RouteArgs& a, int t, bool tok, int lane,
-                                         float (&x)[S]) {
-  const float* row = a.logits + static_cast<size_t>(tok ? t : 0) * a.E;
-#pragma unroll
-  for (int s = 0; s < S; ++s) {
-    const int e = lane + 32 * s;
-    x[s] = (tok && e < a.E) ? __ldg(row + e) : 0.f;
-  }
+// A candidate as one 64-bit word: the logit's key above, the complement of the
+// expert index below. The larger word is the larger logit and, among equal
+// logits, the lower expert; 0 is "no candidate".
+__device__ __forceinline__ uint64_t cand_word(uint32_t key, int e) {
+  return key ? (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e))
+             : 0ull;
 }
 
-// Order-preserving keys of a loaded row; 0 where there is no candidate. NaN
-// counts as -inf; NaN and +-inf set `bad`.
+// Sorts v descending (bitonic network; S a power of two, fixed at compile time).
 template <int S>
-__device__ __forceinline__ void row_keys(const RouteArgs& a, bool tok, int lane, const float (&x)[S],
-                                         uint32_t (&key)[S], bool& bad) {
+__device__ __forceinline__ void sort_desc(uint64_t (&v)[S]) {
 #pragma unroll
-  for (int s = 0; s < S; ++s) {
-    const int e = lane + 32 * s;
-    uint32_t kk = 0;
-    if (tok && e < a.E) {
-      float v = x[s];
-      if (!isfinite(v)) {
-        bad = true;
-        if (isnan(v)) v = -INFINITY;
+  for (int size = 2; size <= S; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < S; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const uint64_t x = v[i], y = v[j];
+          const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
+          // runs of length `size` alternate direction; the last merge is descending
+          const bool desc = (i & size) == 0;
+          v[i] = desc ? hi : lo;
+          v[j] = desc ? lo : hi;
+        }
       }
-      kk = float_key(v);
-    }
-    key[s] = kk;
-  }
 }
 
-// Largest key of one lane not yet taken, and its slot (ascending s: equal keys
-// keep the lower expert index).
-template <int S>
-__device__ __forceinline__ void lane_best(const uint32_t (&key)[S], uint32_t taken, uint32_t& bk,
-                                          int& bs) {
-  bk = 0;
-  bs = 0;
+// Top-k of G tokens at once, each a warp-wide row of E logits held S per lane
+// (expert lane + 32 s). Every lane first sorts its own candidates; then each
+// rank is the largest head of the 32 lane lists (two warp reductions: the key,
+// then the lowest expert among equal keys) and its lane drops that head. The G
+// tokens' rank loops are independent, so their reductions overlap. Lane j ends
+// with rank j of token g, written to the block's choice arrays (expert into sE,
+// logit into sV, at row li[g]); `bad` is set by a non-finite logit (NaN ranks as
+// -inf).
+template <int S, int G>
+__device__ __forceinline__ void select_rows(const RouteArgs& a, int t0, const int* li, int lane,
+                                            int* sE, float* sV, bool& bad) {
+  uint64_t v[G][S];
+  {
+    float x[G][S];   // every row's loads in flight together
 #pragma unroll
-  for (int s = 0; s < S; ++s) {
-    const uint32_t ks = ((taken >> s) & 1u) ? 0u : key[s];
-    if (ks > bk) {
-      bk = ks;
-      bs = s;
+    for (int g = 0; g < G; ++g) {
+      const float* row = a.logits + static_cast<size_t>(t0 + li[g]) * a.E;
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        const int e = lane + 32 * s;
+        x[g][s] = e < a.E ? __ldg(row + e) : 0.f;
+      }
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        const int e = lane + 32 * s;
+        uint32_t kk = 0;
+        if (e < a.E) {
+          float f = x[g][s];
+          if (!isfinite(f)) {
+            bad = true;
+            if (isnan(f)) f = -INFINITY;
+          }
+          kk = float_key(f);
+        }
+        v[g][s] = cand_word(kk, e);
+      }
   }
-}
-
-// Top-k of four tokens' keys at once (rows without candidates hold all-zero
-// keys; their results are not used): rank j of a token is its largest remaining
-// key, the lowest expert index among equal keys, found with two warp reductions.
-// The four tokens' rank loops are independent, so their reductions overlap.
-// Choice j of row q ends in lane (sb + q) * kp + j as (pv, pe).
-template <int S>
-__device__ __forceinline__ void select_topk4(const uint32_t (&k0)[S], const uint32_t (&k1)[S],
-                                             const uint32_t (&k2)[S], const uint32_t (&k3)[S],
-                                             int k, int kp, int sb, int lane, float& pv, int& pe) {
-  uint32_t tk[4] = {0u, 0u, 0u, 0u};   // bit s: key[s] of this lane already chosen
-  uint32_t my_k[4] = {0u, 0u, 0u, 0u};
-  int my_e[4] = {0, 0, 0, 0};
-  for (int j = 0; j < k; ++j) {
-    uint32_t bk[4];
-    int bs[4];
-    lane_best<S>(k0, tk[0], bk[0], bs[0]);
-    lane_best<S>(k1, tk[1], bk[1], bs[1]);
-    lane_best<S>(k2, tk[2], bk[2], bs[2]);
-    lane_best<S>(k3, tk[3], bk[3], bs[3]);
-    uint32_t wk[4], we[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) wk[q] = __reduce_max_sync(kFull, bk[q]);
+  for (int g = 0; g < G; ++g) sort_desc<S>(v[g]);
+  uint32_t vk[G];
+  int ve[G];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      we[q] = __reduce_min_sync(
-          kFull, bk[q] == wk[q] ? static_cast<uint32_t>(lane + 32 * bs[q]) : 0xFFFFFFFFu);
+  for (int g = 0; g < G; ++g) {
+    vk[g] = 0u;
+    ve[g] = 0;
+  }
+  for (int j = 0; j < a.k; ++j) {
+    uint32_t wk[G], wl[G];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (static_cast<int>(we[q] & 31u) == lane) tk[q] |= 1u << (we[q] >> 5);
+    for (int g = 0; g < G; ++g) wk[g] = __reduce_max_sync(kFull, static_cast<uint32_t>(v[g][0] >> 32));
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint32_t hk = static_cast<uint32_t>(v[g][0] >> 32);
+      wl[g] = __reduce_max_sync(kFull, hk == wk[g] ? static_cast<uint32_t>(v[g][0]) : 0u);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint64_t win = (static_cast<uint64_t>(wk[g]) << 32) | wl[g];
+      if (v[g][0] == win) {   // this lane held the chosen candidate: drop it
+#pragma unroll
+        for (int s = 0; s + 1 < S; ++s) v[g][s] = v[g][s + 1];
+        v[g][S - 1] = 0ull;
+      }
       if (lane == j) {
-        my_e[q] = static_cast<int>(we[q]);
-        my_k[q] = wk[q];
+        vk[g] = wk[g];
+        ve[g] = static_cast<int>(0xFFFFFFFFu - wl[g]);
       }
     }
   }
-  // row q's choice j moves from lane j to lane (sb + q) * kp + j
-  const int q = lane / kp - sb;
+  if (lane < a.k) {
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const uint32_t sk = __shfl_sync(kFull, my_k[r], lane % kp);
-    const int se = __shfl_sync(kFull, my_e[r], lane % kp);
-    if (q == r) {
-      pv = key_float(sk);
-      pe = se;
+    for (int g = 0; g < G; ++g) {
+      sE[li[g] * a.k + lane] = ve[g];
+      sV[li[g] * a.k + lane] = key_float(vk[g]);
     }
   }
 }
 
-// Block-wide exclusive scan of two counts per thread (kRouteThreads threads).
+// Selection of the block's tokens li[0..G) (G <= 4), as many rows at once as
+// the registers hold for S.
+template <int S>
+__device__ __forceinline__ void select_block_rows(const RouteArgs& a, int t0, const int (&li)[4],
+                                                  int G, int lane, int* sE, float* sV,
+                                                  bool& bad) {
+  if constexpr (S <= 8) {
+    if (G == 4) select_rows<S, 4>(a, t0, li, lane, sE, sV, bad);
+    else if (G == 3) select_rows<S, 3>(a, t0, li, lane, sE, sV, bad);
+    else if (G == 2) select_rows<S, 2>(a, t0, li, lane, sE, sV, bad);
+    else select_rows<S, 1>(a, t0, li, lane, sE, sV, bad);
+  } else if constexpr (S == 16) {
+    for (int g = 0; g < G; g += 2) {
+      if (g + 1 < G) select_rows<S, 2>(a, t0, li + g, lane, sE, sV, bad);
+      else select_rows<S, 1>(a, t0, li + g, lane, sE, sV, bad);
+    }
+  } else {
+    for (int g = 0; g < G; ++g) select_rows<S, 1>(a, t0, li + g, lane, sE, sV, bad);
+  }
+}
+
+// Block-wide exclusive scan of two counts per thread (kRouteThreads threads), in
+// unsigned arithmetic (wraps rather than overflows on a corrupt workspace).
 // Gives this thread's exclusive prefixes of (x, y) and the block totals.
-__device__ __forceinline__ void block_scan2(int x, int y, int (&ws)[2][kRouteWarps], int& ex,
-                                            int& ey, int& tx, int& ty) {
+__device__ __forceinline__ void block_scan2(uint32_t x, uint32_t y, uint32_t (&ws)[2][kRouteWarps],
+                                            uint32_t& ex, uint32_t& ey, uint32_t& tx,
+                                            uint32_t& ty) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int ix = x, iy = y;
+  uint32_t ix = x, iy = y;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int u = __shfl_up_sync(kFull, ix, off);
-    const int v = __shfl_up_sync(kFull, iy, off);
+    const uint32_t u = __shfl_up_sync(kFull, ix, off);
+    const uint32_t v = __shfl_up_sync(kFull, iy, off);
     if (lane >= off) {
       ix += u;
       iy += v;
@@ -172,7 +188,7 @@ __device__ __forceinline__ void block_scan2(int x, int y, int (&ws)[2][kRouteWar
     ws[1][warp] = iy;
   }
   __syncthreads();
-  int bx = 0, by = 0;
+  uint32_t bx = 0, by = 0;
   tx = 0;
   ty = 0;
 #pragma unroll
@@ -189,133 +205,100 @@ __device__ __forceinline__ void block_scan2(int x, int y, int (&ws)[2][kRouteWar
   __syncthreads();   // ws may be reused
 }
 
-// The routing kernel: one cooperative launch (every block resident at once, so
-// the waits on other blocks always end), one block of kRouteThreads threads
-// per a.tpb tokens. S = logits held per lane (E <= 32 * S).
+// Shared-memory arrays of a routing block over TB tokens (4-byte words).
+struct RouteSmem {
+  int* sE;          // [TB k] expert of each block row (t, j)
+  int* sRank;       // [TB k] rank among the block's rows of that expert
+  float* sV;        // [TB k] logit of each choice
+  int* sCnt;        // [ep]   block counts
+  int* sBase;       // [ep]   rows of each expert in earlier blocks
+  int* sOff;        // [ep + 4] expert totals, then offsets
+  int* sLead;       // [kRouteThreads] group base handed to peers
+  uint32_t* sPart;  // [2][phases][ep] partial sums of the count rows
+};
+
+__host__ __device__ inline int route_ep(int E) { return (E + 3) & ~3; }   // count-row stride
+__host__ __device__ inline int route_phases(int E) {
+  const int groups = route_ep(E) / 4;
+  return groups <= kRouteThreads ? kRouteThreads / groups : 1;
+}
+
+// Dynamic shared memory of a routing block (4-byte words).
+__host__ __device__ inline size_t route_smem_words(int E, int k, int tpb) {
+  const int ep = route_ep(E);
+  return 3 * static_cast<size_t>(tpb) * k + 3 * static_cast<size_t>(ep) + 4 + kRouteThreads +
+         2 * static_cast<size_t>(route_phases(E)) * ep;
+}
+
+__device__ __forceinline__ RouteSmem route_smem(int* smem, const RouteArgs& a) {
+  const int TB = a.tpb, k = a.k, ep = route_ep(a.E);
+  RouteSmem m;
+  m.sE = smem;
+  m.sRank = m.sE + TB * k;
+  m.sV = reinterpret_cast<float*>(m.sRank + TB * k);
+  m.sCnt = reinterpret_cast<int*>(m.sV + TB * k);
+  m.sBase = m.sCnt + ep;
+  m.sOff = m.sBase + ep;
+  m.sLead = m.sOff + ep + 4;
+  m.sPart = reinterpret_cast<uint32_t*>(m.sLead + kRouteThreads);
+  return m;
+}
+
+// The choice of each of the block's nt tokens (experts into sE, logits into
+// sV), then the block's counts (sCnt) and each row's stable rank among the
+// block's rows of its expert (sRank, rows in ascending (t, j) order).
 template <int S>
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a) {
-  extern __shared__ int smem[];
-  __shared__ int s_b;
-  __shared__ uint32_t s_epoch;
-  __shared__ int s_ws[2][kRouteWarps];
+__device__ __forceinline__ void choose_and_rank(const RouteArgs& a, const RouteSmem& m, int t0,
+                                                int nt) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = a.E, k = a.k, TB = a.tpb;
-  int* sE = smem;                      // [TB k] expert of each block row (t, j)
-  int* sRank = sE + TB * k;            // [TB k] rank among the block's rows of that expert
-  int* sCnt = sRank + TB * k;          // [E]    block counts
-  int* sBase = sCnt + E;               // [E]    earlier blocks' counts (lookback)
-  int* sOff = sBase + E;               // [E+1]  expert totals, then offsets
-  int* sLead = sOff + E + 1;           // [kRouteThreads] group base handed to peers
-
-  griddep_launch_dependents();   // the GEMM that follows may start its prologue
-  // launched with programmatic serialization (a one-block grid): the previous
-  // kernel on the stream may still read the arrays this call rewrites
-  griddep_wait();
-  if (tid == 0) {
-    s_b = atomicAdd(&a.ctr[kCtrTicket], 1);   // virtual block id = arrival order
-    s_epoch = static_cast<uint32_t>(a.ctr[kCtrEpoch]);
-  }
-  for (int e = tid; e < E; e += kRouteThreads) sCnt[e] = 0;
-  __syncthreads();
-  const int b = s_b;
-  if (b >= a.nblk) {   // the counters were not zero at launch: refuse to write out of range
-    if (tid == 0) atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);
-    return;
-  }
-  const uint64_t ep = static_cast<uint64_t>(s_epoch) << 32;
-  const int t0 = b * TB;
-  const int nt = max(0, min(TB, a.T - t0));
-
-  // ---- per-token top-k on the fp32 logits, then the weights. The fp64 pipe
-  // is narrow, so the k choices of a pack of P = 32 / kp consecutive tokens
-  // (kp = k rounded up to a power of two) share one pass of fp64 instructions,
-  // token s of the pack in lanes [s kp, s kp + k); pack pk goes to warp
-  // pk % kRouteWarps. Rows are loaded four at a time; each rank is found with
-  // two warp reductions: the largest order-preserving key of the logit, then
-  // the lowest expert index among ties.
-  const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
-  const int P = 32 / kp;
-  constexpr int kPackMax = 4;         // rows held in registers at a time (P may be larger)
-  if (a.ids_given == 1) {
-    // the chosen experts and their weights were written by the fused router:
-    // read the experts; an id out of range is reported and counted as expert 0
-    // so that the permutation stays complete
+  const int E = a.E, k = a.k;
+  for (int e = tid; e < route_ep(E); e += kRouteThreads) m.sCnt[e] = 0;
+  if (a.ids_given != 0) {
+    // the fused router chose the experts (mode 1: with their weights in w;
+    // mode 2: with their logits in w, the weights are computed later). An id
+    // out of range is reported and counted as expert 0 so that the permutation
+    // stays complete.
     for (int i = tid; i < nt * k; i += kRouteThreads) {
-      int e = a.ids[static_cast<size_t>(t0) * k + i];
+      const size_t o = static_cast<size_t>(t0) * k + i;
+      int e = a.ids[o];
       if (e < 0 || e >= E) {
         atomicOr(a.err, MOE_DEVERR_BAD_TILE);
         e = 0;
       }
-      sE[i] = e;
+      m.sE[i] = e;
+      if (a.ids_given == 2) m.sV[i] = a.w[o];
     }
-  }
-  for (int pk = a.ids_given == 1 ? nt : warp; pk * P < nt; pk += kRouteWarps) {
-    const int r0 = pk * P;
-    float pv = -INFINITY;             // this lane's packed choice (token lane / kp, rank lane % kp)
-    int pe = 0;
-    if (a.ids_given == 2) {
-      // the fused router chose the experts and left their logits (descending)
-      // in w: only the weights below remain to be computed
-      const int sp = lane / kp, j = lane % kp, i = r0 + sp;
-      if (j < k && i < nt) {
-        const size_t o = static_cast<size_t>(t0 + i) * k + j;
-        pv = a.w[o];
-        pe = a.ids[o];
-        if (pe < 0 || pe >= E) {
-          atomicOr(a.err, MOE_DEVERR_BAD_TILE);
-          pe = 0;
-        }
+  } else {
+    // warp w takes the block's tokens w, w + 8, w + 16, ..., up to four at a
+    // time with their rank loops interleaved
+    bool bad = false;
+    for (int q0 = 0; warp + kRouteWarps * q0 < nt; q0 += 4) {
+      int li[4];
+      int G = 0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int i = warp + kRouteWarps * (q0 + g);
+        li[g] = i < nt ? i : 0;
+        if (i < nt) G = g + 1;
       }
+      select_block_rows<S>(a, t0, li, G, lane, m.sE, m.sV, bad);
     }
-    for (int sb = 0; a.ids_given == 0 && sb < P && r0 + sb < nt; sb += kPackMax) {
-      auto row_ok = [&](int q) { return sb + q < P && r0 + sb + q < nt; };
-      uint32_t k0[S], k1[S], k2[S], k3[S];   // keys of the rows, 0 = not a candidate
-      {
-        float x0[S], x1[S], x2[S], x3[S];    // all four rows' loads in flight together
-        load_row<S>(a, t0 + r0 + sb, row_ok(0), lane, x0);
-        load_row<S>(a, t0 + r0 + sb + 1, row_ok(1), lane, x1);
-        load_row<S>(a, t0 + r0 + sb + 2, row_ok(2), lane, x2);
-        load_row<S>(a, t0 + r0 + sb + 3, row_ok(3), lane, x3);
-        bool bad = false;
-        row_keys<S>(a, row_ok(0), lane, x0, k0, bad);
-        row_keys<S>(a, row_ok(1), lane, x1, k1, bad);
-        row_keys<S>(a, row_ok(2), lane, x2, k2, bad);
-        row_keys<S>(a, row_ok(3), lane, x3, k3, bad);
-        if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
-      }
-      select_topk4<S>(k0, k1, k2, k3, k, kp, sb, lane, pv, pe);
-    }
-    // renormalised softmax over each token's choices: exp(l_j - l_max) / sum, in fp64
-    const int sp = lane / kp, j = lane % kp;
-    const int i = r0 + sp;
-    const bool act = j < k && i < nt;
-    const float m = __shfl_sync(kFull, pv, sp * kp);   // the token's top logit (rank 0)
-    double ex = act ? exp(static_cast<double>(pv) - static_cast<double>(m)) : 0.0;
-    double sum = ex;
-    for (int off = kp >> 1; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (act) {
-      const size_t o = static_cast<size_t>(t0 + i) * k + j;
-      a.ids[o] = pe;
-      a.w[o] = static_cast<float>(ex / sum);
-      sE[i * k + j] = pe;
-    }
+    if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
   }
   __syncthreads();
-
-  // ---- stable local ranks: rows of the block in ascending (t, j) order
   const int n_ent = nt * k;
   for (int base = 0; base < n_ent; base += kRouteThreads) {
     const int i = base + tid;
     const bool valid = i < n_ent;
-    const int e = valid ? sE[i] : -1 - lane;          // dummies never match each other
+    const int e = valid ? m.sE[i] : -1 - lane;        // dummies never match each other
     const uint32_t peers = __match_any_sync(kFull, e);
     const int leader = __ffs(peers) - 1;
     const int rk = __popc(peers & ((1u << lane) - 1u));
     for (int w = 0; w < kRouteWarps; ++w) {          // warps in order keep the ranks stable
       if (warp == w && valid && lane == leader) {
-        const int bse = sCnt[e];
-        sCnt[e] = bse + __popc(peers);
-        sLead[w * 32 + lane] = bse;
+        const int bse = m.sCnt[e];
+        m.sCnt[e] = bse + __popc(peers);
+        m.sLead[w * 32 + lane] = bse;
       }
       if (base + w * 32 + 32 >= n_ent || w + 1 == kRouteWarps) {
         __syncthreads();
@@ -323,110 +306,79 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
       }
       __syncthreads();
     }
-    if (valid) sRank[i] = sLead[warp * 32 + leader] + rk;
+    if (valid) m.sRank[i] = m.sLead[warp * 32 + leader] + rk;
     __syncthreads();
   }
+}
 
-  // ---- single-pass decoupled lookback over blocks, one column per expert.
-  // Predecessor words are read kLookback at a time (independent loads), then
-  // consumed in order: aggregates are added, an inclusive prefix ends the walk,
-  // a word of another call (epoch) or not yet published is re-read, bounded in
-  // time; after a timeout the partial prefix is published so no block waits on
-  // this one forever.
-  constexpr int kLookback = 16;
-  for (int e = tid; e < E; e += kRouteThreads) {
-    const uint32_t cnt = static_cast<uint32_t>(sCnt[e]);
-    uint64_t* mine = a.lb + static_cast<size_t>(b) * E + e;
-    uint32_t excl = 0;
-    if (b == 0) {
-      st_release64(mine, ep | kLbInclusive | cnt);
-    } else {
-      st_release64(mine, ep | kLbAggregate | cnt);
-      int p = b - 1;
-      uint64_t t_start = 0;
-      uint32_t spins = 0;
-      bool done = false;
-      while (!done && p >= 0) {
-        uint64_t word[kLookback];
-#pragma unroll
-        for (int i = 0; i < kLookback; ++i)
-          word[i] = (p - i >= 0) ? ld_relaxed64(a.lb + static_cast<size_t>(p - i) * E + e)
-                                 : (ep | kLbInclusive);
-        int used = 0;
-#pragma unroll
-        for (int i = 0; i < kLookback; ++i) {
-          if (done || used < i) continue;          // stop at the first word not yet published
-          const uint64_t st = word[i] & kLbStatus;
-          if ((word[i] & ~0xFFFFFFFFull) != ep || st == 0) continue;
-          excl += static_cast<uint32_t>(word[i]) & kLbValueMask;
-          used = i + 1;
-          if (st == kLbInclusive) done = true;
-        }
-        p -= used;
-        if (!done && used < kLookback && p >= 0) {   // a predecessor has not published yet
-          if ((++spins & 15u) == 0) {
-            if (t_start == 0) t_start = globaltimer_ns();
-            else if (globaltimer_ns() - t_start > a.timeout_ns) {
-              atomicOr(a.err, MOE_DEVERR_SCAN_TIMEOUT);
-              break;
-            }
-          }
-        }
-      }
-      st_release64(mine, ep | kLbInclusive | ((excl + cnt) & kLbValueMask));
+// Renormalised softmax over each token's choices from their logits in sV:
+// exp(l_j - l_max) / sum, in fp64, written to w (and, with write_ids, the
+// experts to ids). The fp64 pipe is narrow, so the k choices of a pack of P = 32 / kp
+// consecutive tokens (kp = k rounded up to a power of two) share one pass:
+// token s of the pack in lanes [s kp, s kp + k).
+__device__ __forceinline__ void block_weights(const RouteArgs& a, const RouteSmem& m, int t0,
+                                              int nt, bool write_ids) {
+  if (a.ids_given == 1) return;   // the weights came with the choice
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int k = a.k;
+  const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
+  const int P = 32 / kp;
+  const int sp = lane / kp, j = lane % kp;
+  for (int pk = warp; pk * P < nt; pk += kRouteWarps) {
+    const int i = pk * P + sp;
+    const bool act = j < k && i < nt;
+    const float pv = act ? m.sV[i * k + j] : -INFINITY;
+    const float mx = __shfl_sync(kFull, pv, sp * kp);   // the token's top logit (rank 0)
+    double ex = act ? exp(static_cast<double>(pv) - static_cast<double>(mx)) : 0.0;
+    double sum = ex;
+    for (int off = kp >> 1; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (act) {
+      const size_t o = static_cast<size_t>(t0 + i) * k + j;
+      if (write_ids) a.ids[o] = m.sE[i * k + j];
+      a.w[o] = static_cast<float>(ex / sum);
     }
-    sBase[e] = static_cast<int>(excl);
   }
+}
 
-  // ---- expert totals: the last block's inclusive prefixes (waited for, bounded)
-  const uint64_t* last = a.lb + static_cast<size_t>(a.nblk - 1) * E;
-  for (int e = tid; e < E; e += kRouteThreads) {
-    uint64_t w = 0;
-    uint64_t t_start = 0;
-    for (uint32_t spins = 1;; ++spins) {
-      w = ld_relaxed64(last + e);
-      if ((w & ~0xFFFFFFFFull) == ep && (w & kLbStatus) == kLbInclusive) break;
-      if ((spins & 15u) == 0) {
-        if (t_start == 0) t_start = globaltimer_ns();
-        else if (globaltimer_ns() - t_start > a.timeout_ns) {
-          atomicOr(a.err, MOE_DEVERR_SCAN_TIMEOUT);
-          break;
-        }
-      }
-      __nanosleep(32);
-    }
-    sOff[e] = static_cast<int>(static_cast<uint32_t>(w) & kLbValueMask);
-  }
-  __syncthreads();
-
-  // ---- expert offsets (every block), counts and block map (block 0).
-  // Thread tid owns experts [tid per, tid per + per).
+// Expert offsets from the totals in sOff (every block), counts and block map
+// (block 0), then the scatter of the block's rows to offset + earlier blocks'
+// rows (sBase) + rank. Thread tid owns experts [tid per, tid per + per). A
+// total above T k (only on a corrupt workspace, with the error word set) is
+// clamped, and every write is range-checked.
+__device__ __forceinline__ void place_rows(const RouteArgs& a, const RouteSmem& m, int b, int t0,
+                                           int nt) {
+  __shared__ uint32_t s_ws[2][kRouteWarps];
+  const int tid = threadIdx.x;
+  const int E = a.E, k = a.k;
+  const uint32_t n = static_cast<uint32_t>(a.T) * static_cast<uint32_t>(k);
   const int per = (E + kRouteThreads - 1) / kRouteThreads;
-  int sc = 0, stl = 0;
+  uint32_t sc = 0, stl = 0;
   for (int q = 0; q < per; ++q) {
     const int e = tid * per + q;
     if (e < E) {
-      const int c = sOff[e];
+      const uint32_t c = min(static_cast<uint32_t>(m.sOff[e]), n);
       sc += c;
       stl += (c + a.block_m - 1) / a.block_m;
     }
   }
-  int off, toff, tot_c, tot_t;
+  uint32_t off, toff, tot_c, tot_t;
   block_scan2(sc, stl, s_ws, off, toff, tot_c, tot_t);
+  if (tid == 0 && tot_c != n) atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);
   for (int q = 0; q < per; ++q) {
     const int e = tid * per + q;
     if (e < E) {
-      const int c = sOff[e];
-      sOff[e] = off;
+      const uint32_t c = min(static_cast<uint32_t>(m.sOff[e]), n);
+      m.sOff[e] = static_cast<int>(off);
       if (b == 0) {
-        a.counts[e] = c;
-        a.offsets[e] = off;
-        const int ntl = (c + a.block_m - 1) / a.block_m;
-        for (int s = 0; s < ntl; ++s) {
+        a.counts[e] = static_cast<int>(c);
+        a.offsets[e] = static_cast<int>(off);
+        const uint32_t ntl = (c + a.block_m - 1) / a.block_m;
+        for (uint32_t s = 0; s < ntl; ++s) {
+          if (toff + s >= static_cast<uint32_t>(a.max_tiles)) break;
           int32_t* tl = a.tiles + 3 * static_cast<size_t>(toff + s);
           tl[0] = e;
-          tl[1] = off + s * a.block_m;
-          tl[2] = min(a.block_m, c - s * a.block_m);
+          tl[1] = static_cast<int>(off + s * a.block_m);
+          tl[2] = static_cast<int>(min(static_cast<uint32_t>(a.block_m), c - s * a.block_m));
         }
         toff += ntl;
       }
@@ -434,17 +386,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     }
   }
   if (b == 0 && tid == 0) {
-    a.offsets[E] = tot_c;
-    *a.n_tiles = tot_t;
+    a.offsets[E] = static_cast<int>(tot_c);
+    *a.n_tiles = static_cast<int>(min(tot_t, static_cast<uint32_t>(a.max_tiles)));
   }
   __syncthreads();
-
-  // ---- scatter of this block's rows into their expert groups
-  const long long n = static_cast<long long>(a.T) * k;
+  const int n_ent = nt * k;
   for (int i = tid; i < n_ent; i += kRouteThreads) {
-    const int e = sE[i];
-    const long long pos = static_cast<long long>(sOff[e]) + sBase[e] + sRank[i];
-    if (pos < 0 || pos >= n) {   // only after a failed lookback (error word set)
+    const int e = m.sE[i];
+    const uint32_t pos = static_cast<uint32_t>(m.sOff[e]) + static_cast<uint32_t>(m.sBase[e]) +
+                         static_cast<uint32_t>(m.sRank[i]);
+    if (pos >= n) {   // only on a corrupt workspace (error word set)
       atomicOr(a.err, MOE_DEVERR_BAD_WORKSPACE);
       continue;
     }
@@ -452,18 +403,137 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     a.perm[pos] = r;
     a.inv[r] = static_cast<int32_t>(pos);
   }
+}
 
-  // ---- the last block to finish resets the ticket counters and moves to the
-  // next epoch (the lookback words are never cleared: the epoch retires them)
+// Routing of a batch that one block covers (T <= a.tpb): every step in one
+// block, no other block to wait for. Launched with programmatic serialization:
+// the previous kernel on the stream may still read the arrays this call
+// rewrites until griddep_wait returns.
+template <int S>
+__global__ void __launch_bounds__(kRouteThreads) route_single_kernel(const RouteArgs a) {
+  extern __shared__ int smem[];
+  const RouteSmem m = route_smem(smem, a);
+  griddep_launch_dependents();   // the GEMM that follows may start its prologue
+  griddep_wait();
+  const int nt = max(0, a.T);
+  choose_and_rank<S>(a, m, 0, nt);
+  block_weights(a, m, 0, nt, a.ids_given == 0);
+  for (int e = threadIdx.x; e < a.E; e += kRouteThreads) {
+    m.sBase[e] = 0;
+    m.sOff[e] = m.sCnt[e];
+  }
   __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&a.ctr[kCtrLeave], 1) == a.nblk - 1) {
-      a.ctr[kCtrTicket] = 0;
-      a.ctr[kCtrLeave] = 0;
-      a.ctr[kCtrEpoch] = static_cast<int32_t>(s_epoch + 1u);
+  place_rows(a, m, 0, 0, nt);
+}
+
+// Routing of a larger batch, first of two launches: block b chooses the
+// experts of its a.tpb tokens, counts them and ranks its rows; it publishes its
+// counts as row b of the count rows, the experts in ids, their logits in w
+// (mode 0; mode 2 arrives with them there) and each row's rank in inv.
+template <int S>
+__global__ void __launch_bounds__(kRouteThreads) route_count_kernel(const RouteArgs a) {
+  extern __shared__ int smem[];
+  const RouteSmem m = route_smem(smem, a);
+  const int tid = threadIdx.x, b = blockIdx.x;
+  griddep_wait();
+  const int t0 = b * a.tpb;
+  const int nt = max(0, min(a.tpb, a.T - t0));
+  choose_and_rank<S>(a, m, t0, nt);
+  const int ep = route_ep(a.E);
+  uint4* row = reinterpret_cast<uint4*>(a.rows + static_cast<size_t>(b) * ep);
+  for (int g = tid; g < ep / 4; g += kRouteThreads)
+    row[g] = make_uint4(m.sCnt[4 * g], m.sCnt[4 * g + 1], m.sCnt[4 * g + 2], m.sCnt[4 * g + 3]);
+  const int n_ent = nt * a.k;
+  for (int i = tid; i < n_ent; i += kRouteThreads) {
+    const size_t o = static_cast<size_t>(t0) * a.k + i;
+    if (a.ids_given == 0) {
+      a.ids[o] = m.sE[i];
+      a.w[o] = m.sV[i];
+    }
+    a.inv[o] = m.sRank[i];
+  }
+  // The placing launch may be scheduled only now: placing blocks that wait
+  // while this launch runs (itself scheduled early behind the previous kernel)
+  // were measured to slow it by half.
+  griddep_launch_dependents();
+}
+
+// Second launch: block b reads back its rows' experts, ranks and logits, adds
+// the count rows of all blocks (expert totals) and of the blocks before b (its
+// base), computes its tokens' weights and places its rows. All loads of a
+// thread over the count rows are independent and in flight together.
+__global__ void __launch_bounds__(kRouteThreads) route_place_kernel(const RouteArgs a) {
+  extern __shared__ int smem[];
+  const RouteSmem m = route_smem(smem, a);
+  const int tid = threadIdx.x, b = blockIdx.x;
+  griddep_launch_dependents();   // the GEMM that follows may start its prologue
+  griddep_wait();                // the first launch's writes are visible from here on
+  const int E = a.E, k = a.k;
+  const int t0 = b * a.tpb;
+  const int nt = max(0, min(a.tpb, a.T - t0));
+  const int n_ent = nt * k;
+  for (int i = tid; i < n_ent; i += kRouteThreads) {
+    const size_t o = static_cast<size_t>(t0) * k + i;
+    m.sE[i] = a.ids[o];
+    m.sRank[i] = a.inv[o];
+    if (a.ids_given != 1) m.sV[i] = a.w[o];
+  }
+  const int ep = route_ep(E), groups = ep / 4, phases = route_phases(E);
+  // thread (phase, group) adds rows phase, phase + phases, ... of its four columns
+  const int ph = tid / groups;
+  if (ph < phases) {
+    for (int g = tid - ph * groups; g < groups; g += kRouteThreads) {
+      uint4 pre = make_uint4(0, 0, 0, 0), tot = make_uint4(0, 0, 0, 0);
+      const uint4* col = reinterpret_cast<const uint4*>(a.rows) + g;
+      int r = ph;
+      for (; r + 7 * phases < a.nblk; r += 8 * phases) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(col + static_cast<size_t>(r + u * phases) * groups);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          tot.x += v[u].x;
+          tot.y += v[u].y;
+          tot.z += v[u].z;
+          tot.w += v[u].w;
+          if (r + u * phases < b) {
+            pre.x += v[u].x;
+            pre.y += v[u].y;
+            pre.z += v[u].z;
+            pre.w += v[u].w;
+          }
+        }
+      }
+      for (; r < a.nblk; r += phases) {
+        const uint4 v = __ldcg(col + static_cast<size_t>(r) * groups);
+        tot.x += v.x;
+        tot.y += v.y;
+        tot.z += v.z;
+        tot.w += v.w;
+        if (r < b) {
+          pre.x += v.x;
+          pre.y += v.y;
+          pre.z += v.z;
+          pre.w += v.w;
+        }
+      }
+      reinterpret_cast<uint4*>(m.sPart)[ph * groups + g] = pre;
+      reinterpret_cast<uint4*>(m.sPart + phases * ep)[ph * groups + g] = tot;
     }
   }
+  __syncthreads();
+  block_weights(a, m, t0, nt, false);   // fp64; the experts are in ids already
+  for (int e = tid; e < E; e += kRouteThreads) {
+    uint32_t pre = 0, tot = 0;
+    for (int q = 0; q < phases; ++q) {
+      pre += m.sPart[q * ep + e];
+      tot += m.sPart[(phases + q) * ep + e];
+    }
+    m.sBase[e] = static_cast<int>(pre);
+    m.sOff[e] = static_cast<int>(tot);
+  }
+  __syncthreads();
+  place_rows(a, m, b, t0, nt);
 }
 
 }  // namespace
@@ -474,85 +544,47 @@ RouteWs route_ws_layout(int T, int E, int k) {
   (void)k;
   const size_t nblk = static_cast<size_t>(route_max_blocks(T));
   RouteWs w{};
-  w.ctr = 0;
-  w.lb = 256;
-  w.total = align_up(w.lb + sizeof(uint64_t) * nblk * E, 256);
+  w.rows = 0;
+  w.total = align_up(sizeof(uint32_t) * nblk * route_ep(E), 256);
   return w;
 }
 
 static size_t route_smem_bytes(int E, int k, int tpb) {
-  return sizeof(int) * (2 * static_cast<size_t>(tpb) * k + 3 * static_cast<size_t>(E) + 1 +
-                        kRouteThreads);
-}
-
-// Resident blocks per multiprocessor of a routing kernel for a dynamic shared
-// memory size, remembered per (kernel, size): the query costs host time on
-// every layer call otherwise.
-static cudaError_t route_occupancy(const void* fn, size_t smem, int* per_sm) {
-  struct Entry {
-    const void* fn;
-    size_t smem;
-    int dev, per_sm;
-  };
-  static std::mutex mu;
-  static Entry cache[32];
-  static int n = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    for (int i = 0; i < n; ++i)
-      if (cache[i].fn == fn && cache[i].smem == smem && cache[i].dev == dev) {
-        *per_sm = cache[i].per_sm;
-        return cudaSuccess;
-      }
-  }
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, fn, kRouteThreads, smem);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> g(mu);
-  if (n < 32) cache[n++] = Entry{fn, smem, dev, *per_sm};
-  return cudaSuccess;
+  return sizeof(int) * route_smem_words(E, k, tpb);
 }
 
 template <int S>
-static cudaError_t launch_s(RouteArgs a, int sms, cudaStream_t s) {
+static cudaError_t launch_s(RouteArgs a, cudaStream_t s) {
   // Tokens per block: the multiple of kRouteTokensMin that keeps the grid near
-  // kRouteBlocksTarget blocks (short lookback chains; small blocks spread the
-  // fp64 weight work over more multiprocessors), doubled while the grid would
-  // not be resident at once.
+  // kRouteBlocksTarget blocks (every placing block reads every count row; small
+  // blocks spread the selection and the fp64 weights over more multiprocessors).
   int tpb = kRouteTokensMin;
   while (a.T > tpb * kRouteBlocksTarget) tpb += kRouteTokensMin;
-  for (;;) {
-    const size_t smem = route_smem_bytes(a.E, a.k, tpb);
-    int per_sm = 0;
-    cudaError_t e = route_occupancy(reinterpret_cast<const void*>(route_kernel<S>), smem, &per_sm);
-    if (e != cudaSuccess) return e;
-    const int nblk = a.T > 0 ? (a.T + tpb - 1) / tpb : 1;
-    if (per_sm > 0 && nblk <= per_sm * sms) {
-      a.tpb = tpb;
-      a.nblk = nblk;
-      // one block has no other block to wait for: an ordinary launch, which may
-      // overlap the previous kernel's tail (programmatic serialization)
-      if (nblk == 1)
-        return launch_pdl(route_kernel<S>, dim3(1), dim3(kRouteThreads), smem, s, a);
-      void* args[] = {&a};
-      return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(route_kernel<S>), nblk,
-                                         kRouteThreads, args, smem, s);
-    }
-    if (smem > 48 * 1024) return cudaErrorInvalidValue;
-    tpb *= 2;
+  // at most 48 KB of shared memory per block: larger batches take more blocks
+  while (tpb > kRouteTokensMin && route_smem_bytes(a.E, a.k, tpb) > 48 * 1024)
+    tpb -= kRouteTokensMin;
+  const size_t smem = route_smem_bytes(a.E, a.k, tpb);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  a.tpb = tpb;
+  a.nblk = a.T > 0 ? (a.T + tpb - 1) / tpb : 1;
+  if (a.nblk == 1) {
+    a.tpb = max(a.T, 1);
+    return launch_pdl(route_single_kernel<S>, dim3(1), dim3(kRouteThreads),
+                      route_smem_bytes(a.E, a.k, a.tpb), s, a);
   }
+  cudaError_t e = launch_pdl(route_count_kernel<S>, dim3(a.nblk), dim3(kRouteThreads), smem, s, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(route_place_kernel, dim3(a.nblk), dim3(kRouteThreads), smem, s, a);
 }
 
-cudaError_t launch_route(const RouteArgs& a, int sms, cudaStream_t s) {
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   const int S = (a.E + 31) / 32;
-  if (S <= 1) return launch_s<1>(a, sms, s);
-  if (S <= 2) return launch_s<2>(a, sms, s);
-  if (S <= 4) return launch_s<4>(a, sms, s);
-  if (S <= 8) return launch_s<8>(a, sms, s);
-  if (S <= 16) return launch_s<16>(a, sms, s);
-  return launch_s<32>(a, sms, s);
+  if (S <= 1) return launch_s<1>(a, s);
+  if (S <= 2) return launch_s<2>(a, s);
+  if (S <= 4) return launch_s<4>(a, s);
+  if (S <= 8) return launch_s<8>(a, s);
+  if (S <= 16) return launch_s<16>(a, s);
+  return launch_s<32>(a, s);
 }
 
 }  // namespace moeq4

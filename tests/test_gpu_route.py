@@ -43,10 +43,10 @@ def test_shapes_and_ragged_blocks(T, E, k):
     _check(logits, k, 16)
 
 
-@pytest.mark.parametrize("T,E,k", [(6000, 1024, 8), (40000, 256, 8)])
+@pytest.mark.parametrize("T,E,k", [(6000, 1024, 8), (40000, 256, 8), (100000, 256, 8)])
 def test_large_grids(T, E, k):
-    # more blocks of 8 tokens than the device holds at once: the launch doubles
-    # the tokens per block until the cooperative grid is resident
+    # many tokens per block; at T = 100000 the block's shared memory caps the
+    # tokens per block, so the grid grows past 128 blocks (266)
     rng = np.random.default_rng(T + E)
     logits = rng.standard_normal((T, E)).astype(np.float32)
     _check(logits, k, 128)
@@ -71,29 +71,24 @@ def test_workspace_left_clean_and_reusable():
     cfg = synth.CONFIGS["t512"]
     logits = synth.gen_logits(cfg)
     g1, ws = _check(logits, cfg.k, 128)
-    torch.cuda.synchronize()
-    # the ticket and leave counters open the workspace and are zero again after
-    # a call (the epoch counter and the epoch-tagged lookback words are not)
-    assert int(ws[:8].view(torch.int32).count_nonzero()) == 0
     g2, _ = _check(synth.gen_logits(synth.CONFIGS["t4096"])[:512], cfg.k, 128, ws)
     g3, _ = _check(logits, cfg.k, 128, ws)
     for key in ("ids", "perm", "inv", "tiles"):
         assert np.array_equal(g1[key], g3[key])
 
 
-def test_stale_lookback_words_are_ignored():
-    # words left by an earlier call carry an older epoch: even when they claim
-    # an inclusive prefix they must not be read as this call's
+def test_workspace_contents_do_not_matter():
+    # the count rows may hold anything at launch: the choosing launch writes
+    # every row before the placing launch reads it
     cfg = synth.CONFIGS["t512"]
     logits = synth.gen_logits(cfg)
     g1, ws = _check(logits, cfg.k, 128)
-    epoch = int(ws[8:12].view(torch.int32)[0])
-    assert epoch >= 1
-    stale = ((epoch - 1) << 32) | (2 << 30) | 12345
-    ws[256:].view(torch.int64).fill_(stale)
+    ws.view(torch.int32).fill_(12345)
     g2, _ = _check(logits, cfg.k, 128, ws)
-    for key in ("ids", "perm", "inv", "tiles"):
-        assert np.array_equal(g1[key], g2[key])
+    ws.view(torch.int32).fill_(-1)
+    g3, _ = _check(logits, cfg.k, 128, ws)
+    for key in ("ids", "w", "perm", "inv", "tiles"):
+        assert np.array_equal(g1[key], g2[key]) and np.array_equal(g1[key], g3[key])
 
 
 def test_nonfinite_logit_sets_device_error():

@@ -84,14 +84,11 @@ def test_expert_and_topk_beyond_the_fixed_scratch_are_rejected(T, E, k):
     assert e.value.status == moeq4.MOE_ERR_TOO_LARGE
 
 
-def test_words_of_an_unfinished_call_are_ignored():
-    # A call that did not finish (say, one that raced an overlapping call and
-    # had blocks refuse their tickets) leaves lookback words tagged with the
-    # epoch it ran under, some claiming inclusive prefixes, and the epoch
-    # counter not advanced. Plant exactly that state in the fixed scratch: every
-    # lookback word at the current epoch, marked inclusive with a wrong count,
-    # and dirty ticket and leave counters. The next call must start a new epoch
-    # of its own and route exactly as moe_route does.
+def test_state_of_an_unfinished_call_is_ignored():
+    # A call that did not finish (say, one that raced an overlapping call) can
+    # leave count rows of its own in the fixed scratch. Plant such state, rows
+    # full of wrong counts: the next call writes every row before reading it
+    # and must route exactly as moe_route does.
     cfg = synth.CONFIGS["t512"]
     logits = torch.from_numpy(synth.gen_logits(cfg)).cuda()
     ref = _route_ws(logits, cfg.k, 128)
@@ -104,12 +101,7 @@ def test_words_of_an_unfinished_call_are_ignored():
 
     scratch = torch.as_tensor(_Scratch(), device="cuda")
     torch.cuda.synchronize()
-    epoch = int(scratch[2])
-    scratch[0] = 5                                        # ticket counter
-    scratch[1] = 3                                        # blocks-done counter
-    words = scratch[64:].view(torch.int64)
-    word = ((epoch & 0xFFFFFFFF) << 32) | (2 << 30) | 777  # inclusive, wrong count, current epoch
-    words.fill_(word - (1 << 64) if word >= 1 << 63 else word)
+    scratch.fill_(777)                                    # count rows
     torch.cuda.synchronize()
     for _ in range(2):
         _same(_route_noalloc(logits, cfg.k, 128), ref)
