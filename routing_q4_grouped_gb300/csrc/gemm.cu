@@ -146,14 +146,16 @@ struct Unit {
   bool shared;
 };
 
-// Unit u -> (tile, unit column p). Routed units first, tile-major, then shared
-// (shared tiles of NMAX rows).
+// Unit u -> (tile, unit column p). Shared-expert units first (their full
+// tiles are the heaviest units; at the end of the sequence they made the CTAs
+// that drew them finish last), then routed units, tile-major.
 template <int NMAX>
 __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, Unit& U) {
-  const int n_routed = n_rt * a.n_fb;
-  if (u < n_routed) {
-    const int ti = u / a.n_fb;
-    U.p = u - ti * a.n_fb;
+  const int n_shared = a.n_sh_tiles * a.n_fb_sh;
+  if (u >= n_shared) {
+    const int ur = u - n_shared;
+    const int ti = ur / a.n_fb;
+    U.p = ur - ti * a.n_fb;
     const int32_t* tl = a.tiles + 3 * static_cast<size_t>(ti);
     U.e = __ldg(tl);
     U.row0 = __ldg(tl + 1);
@@ -161,13 +163,12 @@ __device__ __forceinline__ bool decode_unit(const GemmArgs& a, int n_rt, int u, 
     U.shared = false;
     U.K = a.K;
     U.act0 = act_tile_base(U.row0, ti);
-    if (U.e < 0 || U.e >= a.E || U.rows < 1 || U.rows > NMAX || U.row0 < 0 ||
+    if (ti >= n_rt || U.e < 0 || U.e >= a.E || U.rows < 1 || U.rows > NMAX || U.row0 < 0 ||
         static_cast<long long>(U.row0) + U.rows > static_cast<long long>(a.T) * a.k)
       return false;
   } else {
-    const int v = u - n_routed;
-    const int st = v / a.n_fb_sh;
-    U.p = v - st * a.n_fb_sh;
+    const int st = u / a.n_fb_sh;
+    U.p = u - st * a.n_fb_sh;
     U.e = 0;
     U.row0 = st * NMAX;
     U.rows = min(NMAX, a.T - U.row0);
@@ -387,16 +388,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stream (the routing) still runs. A wrong guess only costs an idle
   // memory system some bandwidth.
   if (a.prefetch_guess && warp == kProdWarp0 && lane == 0) {
+    const int n_shared = a.n_sh_tiles * a.n_fb_sh;   // known before the block map
     for (int i = 0; i < 2; ++i) {
       const int u = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-      const int ti = u / a.n_fb;
-      if (ti < a.E) {
-        Unit G{};
-        G.e = ti;
-        G.p = u - ti * a.n_fb;
-        G.K = a.K;
-        G.shared = false;
+      Unit G{};
+      if (u < n_shared) {
+        G.e = 0;
+        G.p = u % a.n_fb_sh;
+        G.K = a.K_sh;
+        G.shared = true;
         prefetch_unit(a, G);
+      } else {
+        const int ti = (u - n_shared) / a.n_fb;
+        if (ti < a.E) {
+          G.e = ti;
+          G.p = (u - n_shared) - ti * a.n_fb;
+          G.K = a.K;
+          G.shared = false;
+          prefetch_unit(a, G);
+        }
       }
     }
   }
