@@ -84,9 +84,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete. Gives up (returns
 // false) when *abort becomes non-zero or after `limit_ns` nanoseconds, so a
 // broken pipeline ends the kernel instead of hanging the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                            const volatile int* abort, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -95,6 +94,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
       if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort, uint64_t limit_ns) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, limit_ns);
 }
 
 // ------------------------------------------- programmatic dependent launch
