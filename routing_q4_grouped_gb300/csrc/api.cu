@@ -331,17 +331,18 @@ moe_status router_impl(const uint16_t* x, const uint16_t* w_router, int32_t T, i
   DevInfo di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   if (T == 0) return MOE_OK;
-  CUtensorMap mx, mw;
-  const CUtensorMapSwizzle SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
-  const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!encode_2d(&mx, BF16, 2, x, d, T, 64, 128, SW128) ||
-      !encode_2d(&mw, BF16, 2, w_router, d, r->E, 64, r->E, SW128))
-    return MOE_ERR_CUDA;
   RouterArgs a{};
   a.T = T;
   a.d = d;
   a.E = r->E;
   a.k = r->k;
+  router_geometry(a);
+  CUtensorMap mx, mw;
+  const CUtensorMapSwizzle SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_2d(&mx, BF16, 2, x, d, T, 64, 128, SW128) ||
+      !encode_2d(&mw, BF16, 2, w_router, d, r->E, 64, a.En, SW128))
+    return MOE_ERR_CUDA;
   a.logits = logits;
   a.ids = r->ids;
   a.w = r->w;

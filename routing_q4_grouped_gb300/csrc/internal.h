@@ -92,11 +92,15 @@ struct RouterArgs {
   uint64_t timeout_ns;
   int defer_weights;        // write the chosen logits into w and leave the weights to the
                             // routing kernel (which spreads the fp64 work over more SMs)
+  int nsplit;               // CTAs per 128-token tile (a cluster), each with E / nsplit experts
+  int En;                   // experts per CTA
+  int stages;               // K-chunk stages of the shared-memory ring
 };
-// TMA maps: x [T][d] bf16 (box 64 x 128), router weights [E][d] bf16 (box 64 x E).
+// Fills nsplit, En and stages for E experts.
+void router_geometry(RouterArgs& a);
+// TMA maps: x [T][d] bf16 (box 64 x 128), router weights [E][d] bf16 (box 64 x En).
 cudaError_t launch_router(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                           cudaStream_t s);
-size_t router_smem_bytes();
 
 // ------------------------------------------------- kernel-native weight layout
 //

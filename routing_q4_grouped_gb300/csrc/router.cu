@@ -6,14 +6,21 @@
 // Lily, Qwen 추론 최적화" (aitrends.kr), sections "Qwen 구조와 Prefill 경로" and
 // "GPU 상주와 메모리 절감": per-token expert selection kept on the GPU).
 //
-// One CTA per 128 tokens, 4 warps. D[tokens, experts] = X[128, d] * Wr[E, d]^T
-// with tcgen05.mma (M = 128 tokens, N = E <= 256, both operands K-major in
-// shared memory, 128-byte swizzle), accumulated over d in tensor memory: lane =
-// token, column = expert. A four-stage ring of K-chunks (64 wide) is filled by
-// TMA (x tile 16 KB + router tile E x 128 B per stage). The epilogue thread of
-// lane t reads its token's E logits from tensor memory 32 at a time, writes them
-// out and keeps a sorted list of the 8 best (order-preserving keys, strict
-// comparison in ascending expert order, so equal logits keep the lower index).
+// A cluster of nsplit CTAs (2 when E > 128 and E is a multiple of 32, else 1)
+// per 128 tokens, 4 warps each; CTA h of the cluster computes the logits of
+// experts [h En, (h + 1) En), En = E / nsplit: D[tokens, experts] = X[128, d] *
+// Wr[En, d]^T with tcgen05.mma (M = 128 tokens, N = En, both operands K-major
+// in shared memory, 128-byte swizzle), accumulated over d in tensor memory:
+// lane = token, column = expert. A ring of K-chunks (64 wide; as many stages as
+// 227 KB hold: 6 for En = 128) is filled by TMA (x tile 16 KB + router tile
+// En x 128 B per stage). The epilogue thread of lane t reads its token's En
+// logits from tensor memory 32 at a time, writes them out and keeps a sorted
+// list of its k best (order-preserving keys, strict comparison in ascending
+// expert order, so equal logits keep the lower index). CTA 1 hands its lists
+// to CTA 0 through distributed shared memory; CTA 0 merges the two sorted
+// lists (CTA 0's experts are the lower ones, so it wins ties) and writes the
+// choice. Splitting the experts doubles the CTAs and deepens each ring: the K
+// loop is bound by the latency of the TMA loads, not by the tensor pipe.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -25,29 +32,93 @@
 namespace moeq4 {
 namespace {
 
-constexpr int kRtThreads = 128;
-constexpr int kRtStages = 4;
+constexpr int kRtThreads = 512;                 // 16 warps: all of them share the epilogue
+constexpr int kRtStagesMax = 6;
 constexpr int kRtTokens = 128;                  // MMA M
 constexpr int kRtABytes = kRtTokens * 128;      // x tile of one K-chunk
-constexpr int kRtBBytes = kRouterMaxE * 128;    // router tile of one K-chunk (at most)
-constexpr int kRtStageBytes = kRtABytes + kRtBBytes;
-constexpr uint32_t kRtTmemCols = 256;
+constexpr size_t kRtSmemMax = 227 * 1024;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 struct RtCtl {
-  uint64_t full[kRtStages];
-  uint64_t empty[kRtStages];
+  uint64_t full[kRtStagesMax];
+  uint64_t empty[kRtStagesMax];
   uint64_t dfull;
   uint32_t tmem_base;
   int abort;
+  int zero;
+  uint32_t peer_ok;                               // the other CTA's epilogue completed
+  uint32_t merge[kRtTokens / 2][2 * kRouterMaxK]; // the other CTA's lists of this CTA's 64
+                                                  // tokens: k keys, then k experts
 };
-constexpr size_t kRtSmem = 1024 + size_t(kRtStages) * kRtStageBytes + sizeof(RtCtl);
+
+__host__ __device__ inline int rt_stage_bytes(int En) { return kRtABytes + En * 128; }
+__host__ __device__ inline uint32_t rt_tmem_cols(int En) {
+  return En <= 32 ? 32u : En <= 64 ? 64u : En <= 128 ? 128u : 256u;
+}
 
 // Order-preserving key of a float (larger float, larger key); NaN ranks as -inf.
 __device__ __forceinline__ uint32_t rt_key(float v) {
   if (isnan(v)) v = -INFINITY;
   const uint32_t u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ double rt_key_val(uint32_t k) {
+  return static_cast<double>(__uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k));
+}
+
+// Inserts (key, e) into a descending list of kRouterMaxK: it passes strictly
+// smaller keys only, so of equal keys the one inserted first stays first.
+__device__ __forceinline__ void rt_insert(uint32_t (&bk)[kRouterMaxK], int (&be)[kRouterMaxK],
+                                          uint32_t key, int e) {
+  if (key > bk[kRouterMaxK - 1]) {
+    bk[kRouterMaxK - 1] = key;
+    be[kRouterMaxK - 1] = e;
+#pragma unroll
+    for (int p = kRouterMaxK - 1; p > 0; --p) {
+      if (bk[p] > bk[p - 1]) {
+        const uint32_t tk = bk[p];
+        bk[p] = bk[p - 1];
+        bk[p - 1] = tk;
+        const int te = be[p];
+        be[p] = be[p - 1];
+        be[p - 1] = te;
+      }
+    }
+  }
+}
+
+// Merges the descending list at `src` (k keys, then k experts, in shared
+// memory) into (bk, be), keeping the first kRouterMaxK. The list in (bk, be)
+// holds the lower experts: on equal keys it goes first when `mine_first`.
+__device__ __forceinline__ void rt_merge(uint32_t (&bk)[kRouterMaxK], int (&be)[kRouterMaxK],
+                                         const uint32_t* src, bool mine_first) {
+  uint32_t mk[kRouterMaxK];
+  int me[kRouterMaxK];
+  int i0 = 0, i1 = 0;
+#pragma unroll
+  for (int i = 0; i < kRouterMaxK; ++i) {
+    uint32_t k0 = 0;
+    int x0 = 0;
+#pragma unroll
+    for (int q = 0; q < kRouterMaxK; ++q) {   // register-array reads at a run-time index
+      if (q == i0) {
+        k0 = bk[q];
+        x0 = be[q];
+      }
+    }
+    const uint32_t k1 = i1 < kRouterMaxK ? src[i1] : 0u;
+    const int x1 = i1 < kRouterMaxK ? static_cast<int>(src[kRouterMaxK + i1]) : 0;
+    const bool take0 = i0 < kRouterMaxK && (mine_first ? k0 >= k1 : k0 > k1);
+    mk[i] = take0 ? k0 : k1;
+    me[i] = take0 ? x0 : x1;
+    i0 += take0 ? 1 : 0;
+    i1 += take0 ? 0 : 1;
+  }
+#pragma unroll
+  for (int i = 0; i < kRouterMaxK; ++i) {
+    bk[i] = mk[i];
+    be[i] = me[i];
+  }
 }
 
 __global__ void __launch_bounds__(kRtThreads, 1)
@@ -56,23 +127,29 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  RtCtl& ctl = *reinterpret_cast<RtCtl*>(smem + kRtStages * kRtStageBytes);
+  const int sb = rt_stage_bytes(a.En);
+  const int ns = a.stages;
+  RtCtl& ctl = *reinterpret_cast<RtCtl*>(smem + static_cast<size_t>(ns) * sb);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.x * kRtTokens;
+  const int half = a.nsplit > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t0 = (blockIdx.x / a.nsplit) * kRtTokens;
+  const int e0 = half * a.En;
   const int nch = a.d / 64;
+  const uint32_t tcols = rt_tmem_cols(a.En);
   if (tid == 0) {
-    for (int s = 0; s < kRtStages; ++s) {
+    for (int s = 0; s < ns; ++s) {
       mbar_init(&ctl.full[s], 1);
       mbar_init(&ctl.empty[s], 1);
     }
     mbar_init(&ctl.dfull, 1);
     ctl.abort = 0;
+    ctl.zero = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW);
   }
   if (warp == 0) {
-    tmem_alloc(&ctl.tmem_base, kRtTmemCols);
+    tmem_alloc(&ctl.tmem_base, tcols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -83,34 +160,36 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const volatile int* abortp = &ctl.abort;
   const uint64_t lim = a.timeout_ns;
   bool ok = true;
+  int issued = 0;   // K-chunks whose loads the producer lane issued
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();   // x rows: read again by the expert FFN
       for (int c = 0; c < nch; ++c) {
-        const int s = c % kRtStages;
-        if (!mbar_wait(&ctl.empty[s], ((c / kRtStages) & 1) ^ 1, abortp, lim)) {
+        const int s = c % ns;
+        if (!mbar_wait(&ctl.empty[s], ((c / ns) & 1) ^ 1, abortp, lim)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * kRtStageBytes;
-        mbar_arrive_expect_tx(&ctl.full[s], kRtABytes + a.E * 128);
+        uint8_t* st = smem + static_cast<size_t>(s) * sb;
+        mbar_arrive_expect_tx(&ctl.full[s], sb);
         tma_load_2d(st, &tmX, &ctl.full[s], 64 * c, t0, pol);
-        tma_load_2d(st + kRtABytes, &tmW, &ctl.full[s], 64 * c, 0, pol);
+        tma_load_2d(st + kRtABytes, &tmW, &ctl.full[s], 64 * c, e0, pol);
+        issued = c + 1;
       }
       if (!ok && atomicExch(&ctl.abort, 1) == 0) atomicOr(a.err, MOE_DEVERR_PIPE_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(128, a.E);
+    const uint32_t idesc = idesc_bf16_f32(128, a.En);
     for (int c = 0; c < nch && ok; ++c) {
-      const int s = c % kRtStages;
-      ok = __all_sync(kFull, mbar_wait(&ctl.full[s], (c / kRtStages) & 1, abortp, lim));
+      const int s = c % ns;
+      ok = __all_sync(kFull, mbar_wait(&ctl.full[s], (c / ns) & 1, abortp, lim));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t sa = smem_u32(smem + s * kRtStageBytes);
+      const uint32_t sa = smem_u32(smem + static_cast<size_t>(s) * sb);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_ss_elect(tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sa + kRtABytes + kk * 32),
@@ -122,28 +201,35 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
 
   // ------------------------------------------------------------------ epilogue
-  // every warp: lanes 32w.. = tokens t0 + 32w..
+  // warp w reads TMEM lane quarter q = w % 4 (tokens t0 + 32q ..) and column
+  // part p = w / 4 (a quarter of the CTA's experts, in multiples of 32); each
+  // thread keeps its token's best k of its part, the four parts meet in shared
+  // memory (the stage ring is free once the MMAs are done)
   ok = __all_sync(kFull, mbar_wait(&ctl.dfull, 0, abortp, lim));
   tc_fence_after();
-  const int t = t0 + warp * 32 + lane;
+  const int q = warp & 3, part = warp >> 2;
+  const int tl = q * 32 + lane;
+  const int t = t0 + tl;
   const bool tok = t < a.T;
-  if (ok) {
-    uint32_t bk[kRouterMaxK];   // best keys, descending (0 = none)
-    int be[kRouterMaxK];
+  const int cw = 32 * ((a.En + 127) / 128);      // columns of a part
+  const int c_lo = part * cw, c_hi = min(a.En, c_lo + cw);
+  uint32_t bk[kRouterMaxK];   // best keys, descending (0 = none)
+  int be[kRouterMaxK];
 #pragma unroll
-    for (int i = 0; i < kRouterMaxK; ++i) {
-      bk[i] = 0u;
-      be[i] = 0;
-    }
+  for (int i = 0; i < kRouterMaxK; ++i) {
+    bk[i] = 0u;
+    be[i] = 0;
+  }
+  if (ok) {
     bool bad = false;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    for (int cc = 0; cc * 32 < a.E; ++cc) {
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    for (int c = c_lo; c < c_hi; c += 32) {
       uint32_t v[32];
-      tmem_ld_32x32b_x32(taddr + cc * 32, v);
+      tmem_ld_32x32b_x32(taddr + c, v);
       tmem_ld_wait();
-      const int nhere = min(32, a.E - cc * 32);   // 16 or 32 (E is a multiple of 16)
+      const int nhere = min(32, c_hi - c);       // 16 or 32 (En is a multiple of 16)
       if (tok && a.logits) {
-        float4* dst = reinterpret_cast<float4*>(a.logits + static_cast<size_t>(t) * a.E + cc * 32);
+        float4* dst = reinterpret_cast<float4*>(a.logits + static_cast<size_t>(t) * a.E + e0 + c);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (4 * i < nhere)
@@ -152,54 +238,86 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       }
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
-        if (jj >= nhere) break;                      // columns past E hold no logits
+        if (jj >= nhere) break;                    // columns past the part hold no logits
         const float f = __uint_as_float(v[jj]);
         bad |= !isfinite(f);
-        const uint32_t key = rt_key(f);
-        if (key > bk[kRouterMaxK - 1]) {
-          // the new entry bubbles up past strictly smaller keys only
-          bk[kRouterMaxK - 1] = key;
-          be[kRouterMaxK - 1] = cc * 32 + jj;
-#pragma unroll
-          for (int p = kRouterMaxK - 1; p > 0; --p) {
-            if (bk[p] > bk[p - 1]) {
-              const uint32_t tk = bk[p];
-              bk[p] = bk[p - 1];
-              bk[p - 1] = tk;
-              const int te = be[p];
-              be[p] = be[p - 1];
-              be[p - 1] = te;
-            }
-          }
-        }
+        rt_insert(bk, be, rt_key(f), e0 + c + jj);
       }
     }
-    auto key_val = [](uint32_t k) {
-      return static_cast<double>(__uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k));
-    };
-    if (tok && a.defer_weights) {
-      if (bad) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
-      int32_t* ids = a.ids + static_cast<size_t>(t) * a.k;
-      float* w = a.w + static_cast<size_t>(t) * a.k;
+    if (tok && bad) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
+  }
+  const bool blk_ok = __syncthreads_and(ok);     // also: every MMA and TMA copy is done
+  if (!blk_ok && tid == 0) {
+    // a pipeline wait ran out: let the copies still in flight land before the
+    // stage ring is reused or the CTA's shared memory goes away (bounded)
+    const int n = issued < ns ? issued : ns;
+    for (int i = 1; i <= n; ++i) {
+      const int c = issued - i;
+      mbar_wait(&ctl.full[c % ns], (c / ns) & 1, &ctl.zero, 20000000ull);
+    }
+  }
+  __syncthreads();
+  uint32_t* parts = reinterpret_cast<uint32_t*>(smem);   // [part][token][2k]
+  if (part > 0) {
+    uint32_t* dst = parts + (static_cast<size_t>(part) * kRtTokens + tl) * (2 * kRouterMaxK);
+#pragma unroll
+    for (int i = 0; i < kRouterMaxK; ++i) {
+      dst[i] = bk[i];
+      dst[kRouterMaxK + i] = static_cast<uint32_t>(be[i]);
+    }
+  }
+  __syncthreads();
+  if (part == 0) {
+    // parts in ascending expert order: on equal keys the earlier part first
+    for (int pp = 1; pp < 4; ++pp)
+      rt_merge(bk, be, parts + (static_cast<size_t>(pp) * kRtTokens + tl) * (2 * kRouterMaxK), true);
+  }
+
+  // ---- the two CTAs of a cluster swap lists: CTA h finishes tokens 64h ..
+  // 64h + 63 (full warps, so each CTA's fp64 work halves), merging its own
+  // list with the other CTA's. One cluster barrier, reached by every thread of
+  // both CTAs whatever happened before.
+  const int mine_lo = a.nsplit > 1 ? half * (kRtTokens / 2) : 0;
+  const int mine_n = a.nsplit > 1 ? kRtTokens / 2 : kRtTokens;
+  bool write = blk_ok;
+  if (a.nsplit > 1) {
+    const int other = half ^ 1;
+    const int olo = other * (kRtTokens / 2);
+    if (part == 0 && tl >= olo && tl < olo + kRtTokens / 2) {
+      const uint32_t dst = mapa_shared(smem_u32(&ctl.merge[tl - olo][0]), other);
+#pragma unroll
+      for (int i = 0; i < kRouterMaxK; ++i) {
+        st_cluster_u32(dst + 4 * i, bk[i]);
+        st_cluster_u32(dst + 4 * (kRouterMaxK + i), static_cast<uint32_t>(be[i]));
+      }
+    }
+    if (tid == 0) st_cluster_u32(mapa_shared(smem_u32(&ctl.peer_ok), other), blk_ok ? 1u : 0u);
+    cluster_sync_all();
+    write = blk_ok && ctl.peer_ok != 0;
+    if (write && part == 0 && tl >= mine_lo && tl < mine_lo + mine_n)
+      rt_merge(bk, be, &ctl.merge[tl - mine_lo][0], half == 0);
+  }
+
+  if (write && part == 0 && tok && tl >= mine_lo && tl < mine_lo + mine_n) {
+    int32_t* ids = a.ids + static_cast<size_t>(t) * a.k;
+    float* w = a.w + static_cast<size_t>(t) * a.k;
+    if (a.defer_weights) {
 #pragma unroll
       for (int i = 0; i < kRouterMaxK; ++i)
         if (i < a.k) {
           ids[i] = be[i];
-          w[i] = static_cast<float>(key_val(bk[i]));   // the chosen logit itself
+          w[i] = static_cast<float>(rt_key_val(bk[i]));   // the chosen logit itself
         }
-    } else if (tok) {
-      if (bad) atomicOr(a.err, MOE_DEVERR_NONFINITE_LOGIT);
+    } else {
       // renormalised softmax over the chosen logits: exp(l_j - l_0) / sum, in fp64
-      const double m = key_val(bk[0]);
+      const double m = rt_key_val(bk[0]);
       double ex[kRouterMaxK];
       double sum = 0.0;
 #pragma unroll
       for (int i = 0; i < kRouterMaxK; ++i) {
-        ex[i] = i < a.k ? exp(key_val(bk[i]) - m) : 0.0;
+        ex[i] = i < a.k ? exp(rt_key_val(bk[i]) - m) : 0.0;
         sum += ex[i];
       }
-      int32_t* ids = a.ids + static_cast<size_t>(t) * a.k;
-      float* w = a.w + static_cast<size_t>(t) * a.k;
 #pragma unroll
       for (int i = 0; i < kRouterMaxK; ++i)
         if (i < a.k) {
@@ -213,13 +331,21 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kRtTmemCols);
+    tmem_dealloc(tmem, tcols);
   }
 }
 
+size_t rt_ctl_bytes() { return sizeof(RtCtl); }
+
 }  // namespace
 
-size_t router_smem_bytes() { return kRtSmem; }
+void router_geometry(RouterArgs& a) {
+  a.nsplit = (a.E > 128 && a.E % 32 == 0) ? 2 : 1;
+  a.En = a.E / a.nsplit;
+  const size_t room = kRtSmemMax - 1024 - rt_ctl_bytes();
+  const int st = static_cast<int>(room / static_cast<size_t>(rt_stage_bytes(a.En)));
+  a.stages = st < kRtStagesMax ? st : kRtStagesMax;
+}
 
 cudaError_t launch_router(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                           cudaStream_t s) {
@@ -233,13 +359,34 @@ cudaError_t launch_router(const RouterArgs& a, const CUtensorMap& tmX, const CUt
     std::lock_guard<std::mutex> g(mu);
     if (!done[dev]) {
       e = cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kRtSmem));
+                               static_cast<int>(kRtSmemMax));
       if (e != cudaSuccess) return e;
       done[dev] = true;
     }
   }
-  const int grid = (a.T + kRtTokens - 1) / kRtTokens;
-  return launch_pdl(router_topk_kernel, dim3(grid), dim3(kRtThreads), kRtSmem, s, tmX, tmW, a);
+  if (a.stages < 2) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + static_cast<size_t>(a.stages) * rt_stage_bytes(a.En) + rt_ctl_bytes();
+  const int tiles = (a.T + kRtTokens - 1) / kRtTokens;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * a.nsplit);
+  cfg.blockDim = dim3(kRtThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (a.nsplit > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = a.nsplit;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, router_topk_kernel, tmX, tmW, a);
 }
 
 }  // namespace moeq4

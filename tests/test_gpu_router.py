@@ -80,6 +80,33 @@ def test_router_small_expert_counts_and_ties():
         assert np.array_equal(g["w"].view(np.uint32), r.w.view(np.uint32))
 
 
+@pytest.mark.parametrize("E", [128, 160, 240, 256])
+def test_router_expert_halves_and_cross_half_ties(E):
+    # E = 160 and 256 split the experts over a cluster of two CTAs (80 / 128
+    # each); 128 and 240 run one CTA per token tile (6 and 4 ring stages). Router
+    # rows copied across the halves give equal logits in both CTAs: the lower
+    # expert index must still come first.
+    cfg = dataclasses.replace(synth.CONFIGS["t512"], E=E)
+    x = synth.gen_x(cfg, 300)
+    wr = synth.gen_router(cfg)
+    wr[E - 1] = wr[0]
+    wr[E // 2] = wr[1]
+    wr[E // 2 + 3] = wr[E // 2 - 2]
+    out, lg, err = _router_gpu(x, wr, cfg.k)
+    assert err == 0
+    _check_logits(lg, x, wr)
+    assert np.array_equal(lg[:, E - 1], lg[:, 0]) and np.array_equal(lg[:, E // 2], lg[:, 1])
+    r = O.route(lg, cfg.k, 128)
+    g = route_np(out)
+    assert np.array_equal(g["ids"], r.ids)
+    assert np.array_equal(g["w"].view(np.uint32), r.w.view(np.uint32))
+    # the copies make some tokens choose a duplicated pair: both members, lower first
+    both = np.isin(r.ids, [0]).any(axis=1) & np.isin(r.ids, [E - 1]).any(axis=1)
+    for t in np.nonzero(both)[0]:
+        row = list(r.ids[t])
+        assert row.index(0) < row.index(E - 1)
+
+
 @pytest.mark.parametrize("name,T", [("t4096", 4096), ("skew", 2048)])
 def test_routing_from_router_ids(name, T):
     cfg = synth.CONFIGS[name]
