@@ -7,20 +7,23 @@
 // "GPU 상주와 메모리 절감": per-token expert selection kept on the GPU).
 //
 // A cluster of nsplit CTAs (2 when E > 128 and E is a multiple of 32, else 1)
-// per 128 tokens, 4 warps each; CTA h of the cluster computes the logits of
+// per 128 tokens, 16 warps each; CTA h of the cluster computes the logits of
 // experts [h En, (h + 1) En), En = E / nsplit: D[tokens, experts] = X[128, d] *
 // Wr[En, d]^T with tcgen05.mma (M = 128 tokens, N = En, both operands K-major
 // in shared memory, 128-byte swizzle), accumulated over d in tensor memory:
 // lane = token, column = expert. A ring of K-chunks (64 wide; as many stages as
 // 227 KB hold: 6 for En = 128) is filled by TMA (x tile 16 KB + router tile
-// En x 128 B per stage). The epilogue thread of lane t reads its token's En
-// logits from tensor memory 32 at a time, writes them out and keeps a sorted
-// list of its k best (order-preserving keys, strict comparison in ascending
-// expert order, so equal logits keep the lower index). CTA 1 hands its lists
-// to CTA 0 through distributed shared memory; CTA 0 merges the two sorted
-// lists (CTA 0's experts are the lower ones, so it wins ties) and writes the
-// choice. Splitting the experts doubles the CTAs and deepens each ring: the K
-// loop is bound by the latency of the TMA loads, not by the tensor pipe.
+// En x 128 B per stage); warp 0 issues the loads, warp 1 the MMAs.
+//
+// Epilogue, all 16 warps: warp w reads lane quarter w % 4 and a quarter of the
+// CTA's experts, writes those logits and keeps each token's k best of them (a
+// sorted list; a new key passes strictly smaller keys only, and experts come in
+// ascending order, so equal logits keep the lower index). The four lists of a
+// token meet in shared memory; then the two CTAs of a cluster swap, through
+// distributed shared memory, the lists of the tokens the other one finishes:
+// CTA h merges and writes tokens 64h .. 64h + 63 (CTA 0's experts are the lower
+// ones and win ties). Splitting the experts doubles the CTAs and deepens each
+// ring; splitting the tokens halves each SM's share of the fp64 weights.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -31,6 +34,29 @@
 
 namespace moeq4 {
 namespace {
+
+// Cluster helpers (distributed shared memory and the cluster barrier).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address in CTA `rank` of this cluster of the shared-memory word at `saddr`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Every thread of every CTA of the cluster, once: writes to other CTAs' shared
+// memory before it are visible to their reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 constexpr int kRtThreads = 512;                 // 16 warps: all of them share the epilogue
 constexpr int kRtStagesMax = 6;
