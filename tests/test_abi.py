@@ -56,6 +56,19 @@ def test_host_side_sizes(L):
     assert "workspace" in L.status_string(-3)
 
 
+def test_route_workspace_is_one_count_row_per_block(L):
+    # the routing scratch holds one row of per-expert counts (uint32, rows padded
+    # to 4 experts for 16-byte loads) per block of at least 8 tokens, and nothing
+    # else: there are no counters to zero between calls
+    def expect(T, E):
+        blocks = max(1, -(-T // 8))
+        rows = blocks * (-(-E // 4) * 4) * 4
+        return -(-rows // 256) * 256
+    for T, E in [(0, 256), (1, 256), (8, 256), (9, 256), (4096, 256), (100000, 256),
+                 (300, 1000), (5, 17)]:
+        assert L.moe_route_workspace_size(T, E, 8) == expect(T, E), (T, E)
+
+
 def test_router_and_prefetch_arguments_rejected_on_host(L):
     lib = L.lib()
     fake = 1 << 20
