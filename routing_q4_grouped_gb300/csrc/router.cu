@@ -6,24 +6,25 @@
 // Lily, Qwen 추론 최적화" (aitrends.kr), sections "Qwen 구조와 Prefill 경로" and
 // "GPU 상주와 메모리 절감": per-token expert selection kept on the GPU).
 //
-// A cluster of nsplit CTAs (2 when E > 128 and E is a multiple of 32, else 1)
-// per 128 tokens, 16 warps each; CTA h of the cluster computes the logits of
+// A cluster of nsplit CTAs (4 when E >= 256 is a multiple of 64, 2 when E >= 128
+// is a multiple of 32, else 1) per 128 tokens, 16 warps each; CTA h of the cluster computes the logits of
 // experts [h En, (h + 1) En), En = E / nsplit: D[tokens, experts] = X[128, d] *
 // Wr[En, d]^T with tcgen05.mma (M = 128 tokens, N = En, both operands K-major
 // in shared memory, 128-byte swizzle), accumulated over d in tensor memory:
 // lane = token, column = expert. A ring of K-chunks (64 wide; as many stages as
-// 227 KB hold: 6 for En = 128) is filled by TMA (x tile 16 KB + router tile
+// 227 KB hold, at most 8) is filled by TMA (x tile 16 KB + router tile
 // En x 128 B per stage); warp 0 issues the loads, warp 1 the MMAs.
 //
 // Epilogue, all 16 warps: warp w reads lane quarter w % 4 and a quarter of the
 // CTA's experts, writes those logits and keeps each token's k best of them (a
 // sorted list; a new key passes strictly smaller keys only, and experts come in
 // ascending order, so equal logits keep the lower index). The four lists of a
-// token meet in shared memory; then the two CTAs of a cluster swap, through
-// distributed shared memory, the lists of the tokens the other one finishes:
-// CTA h merges and writes tokens 64h .. 64h + 63 (CTA 0's experts are the lower
-// ones and win ties). Splitting the experts doubles the CTAs and deepens each
-// ring; splitting the tokens halves each SM's share of the fp64 weights.
+// token meet in shared memory; then every CTA of a cluster sends, through
+// distributed shared memory, its list of each token to the CTA that finishes
+// it: CTA h merges the lists of tokens [h n, (h + 1) n), n = 128 / nsplit, in
+// ascending CTA order (lower experts first on equal keys) and writes them.
+// Splitting the experts multiplies the CTAs, shrinks what each SM streams and
+// deepens each ring; splitting the tokens shares out the fp64 weights.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -58,8 +59,31 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// One 64-wide K-chunk (4 K-steps of 16) of D[tokens, experts] += A B^T, both
+// operands in shared memory (descriptors a, b; 32-byte K steps), issued by one
+// elected lane of a converged warp from one asm block: issued one by one
+// behind separate elections the MMAs cost ~110 cycles each and set the pace
+// of the K loop. The first step accumulates only if `accumulate` is non-zero.
+__device__ __forceinline__ void rt_mma_chunk_elect(uint32_t d, uint64_t a, uint64_t b,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.u64 a1, %1, 2;\n\tadd.u64 a2, %1, 4;\n\tadd.u64 a3, %1, 6;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, 1;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+constexpr int kRtSplitMax = 4;                  // CTAs per cluster at most
 constexpr int kRtThreads = 512;                 // 16 warps: all of them share the epilogue
-constexpr int kRtStagesMax = 6;
+constexpr int kRtStagesMax = 8;
 constexpr int kRtTokens = 128;                  // MMA M
 constexpr int kRtABytes = kRtTokens * 128;      // x tile of one K-chunk
 constexpr size_t kRtSmemMax = 227 * 1024;
@@ -72,14 +96,17 @@ struct RtCtl {
   uint32_t tmem_base;
   int abort;
   int zero;
-  uint32_t peer_ok;                               // the other CTA's epilogue completed
-  uint32_t merge[kRtTokens / 2][2 * kRouterMaxK]; // the other CTA's lists of this CTA's 64
-                                                  // tokens: k keys, then k experts
+  uint32_t peer_ok[kRtSplitMax];                  // CTA s's epilogue completed
+  uint32_t merge[kRtTokens][2 * kRouterMaxK];     // lists of this CTA's tokens by source CTA:
+                                                  // [s * tokens-per-CTA + token][k keys, k experts]
 };
 
 __host__ __device__ inline int rt_stage_bytes(int En) { return kRtABytes + En * 128; }
+// Tensor-memory columns: the accumulator's En plus the 32 that the epilogue's
+// last 32-column load of a part may reach past it, rounded up to a power of two.
 __host__ __device__ inline uint32_t rt_tmem_cols(int En) {
-  return En <= 32 ? 32u : En <= 64 ? 64u : En <= 128 ? 128u : 256u;
+  const int need = En + 32;
+  return need <= 32 ? 32u : need <= 64 ? 64u : need <= 128 ? 128u : need <= 256 ? 256u : 512u;
 }
 
 // Order-preserving key of a float (larger float, larger key); NaN ranks as -inf.
@@ -216,10 +243,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + static_cast<size_t>(s) * sb);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ss_elect(tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sa + kRtABytes + kk * 32),
-                     idesc, (c | kk) != 0);
+      rt_mma_chunk_elect(tmem, sdesc_k_sw128(sa), sdesc_k_sw128(sa + kRtABytes), idesc, c != 0);
       mma_commit_elect(&ctl.empty[s]);
     }
     if (ok) mma_commit_elect(&ctl.dfull);
@@ -237,7 +261,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const int tl = q * 32 + lane;
   const int t = t0 + tl;
   const bool tok = t < a.T;
-  const int cw = 32 * ((a.En + 127) / 128);      // columns of a part
+  const int cw = 16 * ((a.En + 63) / 64);        // columns of a part (a quarter, rounded up to 16)
   const int c_lo = part * cw, c_hi = min(a.En, c_lo + cw);
   uint32_t bk[kRouterMaxK];   // best keys, descending (0 = none)
   int be[kRouterMaxK];
@@ -299,29 +323,41 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       rt_merge(bk, be, parts + (static_cast<size_t>(pp) * kRtTokens + tl) * (2 * kRouterMaxK), true);
   }
 
-  // ---- the two CTAs of a cluster swap lists: CTA h finishes tokens 64h ..
-  // 64h + 63 (full warps, so each CTA's fp64 work halves), merging its own
-  // list with the other CTA's. One cluster barrier, reached by every thread of
-  // both CTAs whatever happened before.
-  const int mine_lo = a.nsplit > 1 ? half * (kRtTokens / 2) : 0;
-  const int mine_n = a.nsplit > 1 ? kRtTokens / 2 : kRtTokens;
+  // ---- the CTAs of a cluster share out the tokens: CTA h finishes tokens
+  // [h n, (h + 1) n), n = 128 / nsplit (full warps, so each SM's fp64 work
+  // shrinks too), merging the nsplit lists of each of them in ascending CTA
+  // order (lower experts first on equal keys). Every CTA writes its list of each
+  // token into the owner's merge buffer, then one cluster barrier, reached by
+  // every thread of every CTA whatever happened before.
+  const int mine_n = kRtTokens / a.nsplit;
+  const int mine_lo = half * mine_n;
   bool write = blk_ok;
   if (a.nsplit > 1) {
-    const int other = half ^ 1;
-    const int olo = other * (kRtTokens / 2);
-    if (part == 0 && tl >= olo && tl < olo + kRtTokens / 2) {
-      const uint32_t dst = mapa_shared(smem_u32(&ctl.merge[tl - olo][0]), other);
+    if (part == 0) {
+      const int owner = tl / mine_n;
+      const uint32_t dst = mapa_shared(
+          smem_u32(&ctl.merge[half * mine_n + (tl - owner * mine_n)][0]), static_cast<uint32_t>(owner));
 #pragma unroll
       for (int i = 0; i < kRouterMaxK; ++i) {
         st_cluster_u32(dst + 4 * i, bk[i]);
         st_cluster_u32(dst + 4 * (kRouterMaxK + i), static_cast<uint32_t>(be[i]));
       }
     }
-    if (tid == 0) st_cluster_u32(mapa_shared(smem_u32(&ctl.peer_ok), other), blk_ok ? 1u : 0u);
+    if (tid < a.nsplit)
+      st_cluster_u32(mapa_shared(smem_u32(&ctl.peer_ok[half]), static_cast<uint32_t>(tid)),
+                     blk_ok ? 1u : 0u);
     cluster_sync_all();
-    write = blk_ok && ctl.peer_ok != 0;
-    if (write && part == 0 && tl >= mine_lo && tl < mine_lo + mine_n)
-      rt_merge(bk, be, &ctl.merge[tl - mine_lo][0], half == 0);
+    for (int s = 0; s < a.nsplit; ++s) write = write && ctl.peer_ok[s] != 0;
+    if (write && part == 0 && tl >= mine_lo && tl < mine_lo + mine_n) {
+      const uint32_t* l0 = &ctl.merge[tl - mine_lo][0];   // source CTA 0's list
+#pragma unroll
+      for (int i = 0; i < kRouterMaxK; ++i) {
+        bk[i] = l0[i];
+        be[i] = static_cast<int>(l0[kRouterMaxK + i]);
+      }
+      for (int s = 1; s < a.nsplit; ++s)
+        rt_merge(bk, be, &ctl.merge[s * mine_n + (tl - mine_lo)][0], true);
+    }
   }
 
   if (write && part == 0 && tok && tl >= mine_lo && tl < mine_lo + mine_n) {
@@ -366,7 +402,8 @@ size_t rt_ctl_bytes() { return sizeof(RtCtl); }
 }  // namespace
 
 void router_geometry(RouterArgs& a) {
-  a.nsplit = (a.E > 128 && a.E % 32 == 0) ? 2 : 1;
+  // experts per CTA: a multiple of 16 (the MMA width step), at least 64
+  a.nsplit = (a.E >= 256 && a.E % 64 == 0) ? 4 : (a.E >= 128 && a.E % 32 == 0) ? 2 : 1;
   a.En = a.E / a.nsplit;
   const size_t room = kRtSmemMax - 1024 - rt_ctl_bytes();
   const int st = static_cast<int>(room / static_cast<size_t>(rt_stage_bytes(a.En)));
