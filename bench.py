@@ -52,10 +52,18 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer prefill tokens/s at T=4096; grouped-GEMM % of GB300 BF16 TC peak"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# stage events 0..5 bracket: routing (one kernel; events 1 and 2 coincide), gate/up
-# GEMM, down GEMM with the combine and the bf16 output (events 4 and 5 coincide)
+# stage events 0..5 bracket: routing (one or two launches; events 1 and 2 coincide),
+# gate/up GEMM, down GEMM with the combine and the bf16 output (events 4 and 5
+# coincide)
 STAGES = ["route", None, "gemm_gate_up_swiglu", "gemm_down_combine", None]
-LAUNCHES_PER_LAYER = 3
+
+
+def launches_per_layer(T, decode=False):
+    """Kernel launches of one moe_layer call: routing takes one launch when one
+    block covers the batch (T <= 8) and two otherwise; the FFN two (the grouped
+    GEMM's passes) or three on the small-batch path (gate/up, down, bf16 output)."""
+    return (1 if T <= 8 else 2) + (3 if decode else 2)
+
 KERNEL_SOURCES = ["gemm.cu", "dequant.cuh", "ptx.cuh"]
 
 
@@ -515,7 +523,7 @@ def measure_workload(name, args, world, rank, local, steps, warmup, sets_n, cloc
         "touched_experts": touched,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "clocks": clk, "weight_bytes": weight_bytes, "launches": LAUNCHES_PER_LAYER * steps,
+        "clocks": clk, "weight_bytes": weight_bytes, "launches": launches_per_layer(T) * steps,
     }
 
 
@@ -571,7 +579,8 @@ def measure_router(name, steps, warmup):
             "l2": "flushed (256 MB write) before every timed call",
             "layer_from_hidden_states": {"value": T / (ms_layer * 1e-3), "unit": UNIT,
                                          "ms_per_step": ms_layer},
-            "launches": 5 * steps}
+            # the router alone, then the router + routing from its choice + the FFN
+            "launches": (1 + 1 + launches_per_layer(T)) * steps}
 
 
 def measure_decode(steps, warmup):
@@ -649,7 +658,9 @@ def measure_decode(steps, warmup):
                          "achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "frac": t_roof / (ms * 1e-3),
                          "frac_graph": t_roof / (ms_g * 1e-3) if ms_g else None,
                          "peak_gbs": pk["hbm_gbs"]}}
-        launches += 4 * steps
+        # stream launches, and the same kernels again as graph replays
+        per = launches_per_layer(T, decode=T <= 2)
+        launches += per * steps * (2 if ms_g else 1)
     out["launches"] = launches
     return out
 
@@ -934,7 +945,7 @@ def run_chunked(args):
                 "h2d_bytes_per_step": x0.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2},
         "clocks": clk,
-        "gpu_launches": (LAUNCHES_PER_LAYER * L + (L - 1) + (L if prefetch_bytes else 0))
+        "gpu_launches": (launches_per_layer(C) * L + (L - 1) + (L if prefetch_bytes else 0))
                         * nch * args.steps,
     }
     if rank == 0:

@@ -178,7 +178,7 @@ moe_status route_impl(const float* logits, const moe_route_out* r, void* ws, siz
   stage_mark(0, s);
   if (launch_route(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   stage_mark(1, s);
-  stage_mark(2, s);   // (one routing kernel: stages 1 and 2 coincide)
+  stage_mark(2, s);   // (routing is one step: stages 1 and 2 coincide)
   return MOE_OK;
 }
 
