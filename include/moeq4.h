@@ -204,8 +204,9 @@ moe_status moe_route_noalloc(const float* logits, const moe_route_out* out, void
  *   logits    fp32 [T][E] (device) or NULL when only the choice is wanted
  *   out       only ids, w and err are written; T, E, k describe them
  * Limits: E % 16 == 0, E <= 256, k <= 8, d % 64 == 0. Non-finite logits rank as
- * -inf and set MOE_DEVERR_NONFINITE_LOGIT. One kernel launch (tcgen05, 128 tokens
- * per CTA). T = 0 launches nothing. */
+ * -inf and set MOE_DEVERR_NONFINITE_LOGIT. One kernel launch (tcgen05; a cluster
+ * of 4, 2 or 1 CTAs per 128 tokens, each with a share of the experts, merging
+ * their lists through distributed shared memory). T = 0 launches nothing. */
 moe_status moe_router_topk(const uint16_t* x, const uint16_t* w_router, int32_t T, int32_t d,
                            float* logits, const moe_route_out* out, void* stream);
 
