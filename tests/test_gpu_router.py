@@ -107,6 +107,22 @@ def test_router_expert_halves_and_cross_half_ties(E):
         assert row.index(0) < row.index(E - 1)
 
 
+@pytest.mark.parametrize("k", [1, 2, 6])
+def test_router_clusters_with_fewer_choices(k):
+    # E = 256: four CTAs per token tile, each keeping its best k of 64 experts;
+    # the merged lists must still give the k largest of all 256
+    cfg = synth.CONFIGS["t512"]
+    x = synth.gen_x(cfg, 200)
+    wr = synth.gen_router(cfg)
+    out, lg, err = _router_gpu(x, wr, k)
+    assert err == 0
+    _check_logits(lg, x, wr)
+    r = O.route(lg, k, 128)
+    g = route_np(out)
+    assert np.array_equal(g["ids"], r.ids)
+    assert np.array_equal(g["w"].view(np.uint32), r.w.view(np.uint32))
+
+
 @pytest.mark.parametrize("name,T", [("t4096", 4096), ("skew", 2048)])
 def test_routing_from_router_ids(name, T):
     cfg = synth.CONFIGS[name]
