@@ -219,7 +219,8 @@ moe_status moe_route_ids(const moe_route_out* out, void* ws, size_t ws_bytes, vo
 /* The layer from hidden states: moe_router_topk, moe_route_ids and
  * moe_expert_ffn on one stream, no host sync. logits may be NULL; ws of
  * moe_layer_workspace_size(...) bytes, zero-filled before first use. The
- * router limits above apply. */
+ * router limits above apply. Every host-side check of the three steps runs
+ * before the first launch: a rejected call enqueues nothing. */
 moe_status moe_layer_router(const uint16_t* x, const uint16_t* w_router, int32_t T,
                             const moe_q4_packed* W, float* logits, const moe_route_out* r,
                             uint16_t* y, void* ws, size_t ws_bytes, void* stream);
@@ -255,7 +256,8 @@ moe_status moe_expert_ffn_decode(const uint16_t* x, int32_t T, int32_t d,
  *   x bf16 [T][d], logits fp32 [T][E]; r receives the routing result; y bf16 [T][d].
  *   ws of moe_layer_workspace_size(...) bytes, zero-filled before first use.
  * T = 0 is allowed (the routing result is the empty one; x, logits and y may
- * be NULL). */
+ * be NULL). Every host-side check of both steps runs before the first launch:
+ * a rejected call enqueues nothing. */
 moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const moe_q4_packed* W,
                      const moe_route_out* r, uint16_t* y, void* ws, size_t ws_bytes,
                      void* stream);

@@ -479,6 +479,7 @@ moe_status moe_layer(const uint16_t* x, const float* logits, int32_t T, const mo
   // validate the FFN arguments before anything is enqueued
   if ((st = check_packed(W)) != MOE_OK) return st;
   if (T > 0 && (!x || !y)) return MOE_ERR_ARG;   // x, y (and logits) may be NULL when T == 0
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_ALIGN;
   if (W->E != r->E) return MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = route_impl(logits, r, ws, rsz, s)) != MOE_OK) return st;
@@ -519,6 +520,7 @@ moe_status moe_layer_router(const uint16_t* x, const uint16_t* w_router, int32_t
   if ((st = check_packed(W)) != MOE_OK) return st;
   if ((st = check_route_out(r)) != MOE_OK) return st;
   if (T > 0 && (!x || !y)) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_ALIGN;
   if (W->E != r->E) return MOE_ERR_SHAPE;
   if (r->E % 16 || r->E > kRouterMaxE || r->k > kRouterMaxK) return MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

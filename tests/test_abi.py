@@ -155,5 +155,15 @@ def test_ffn_and_layer_arguments_rejected_on_host(L):
     assert lay(fake, fake, 16, fake, fake, 64) == -3          # workspace too small
     assert lay(None, fake, 16, fake, fake, big) == -1         # x NULL with T > 0
     assert lay(fake, fake, 16, None, fake, big) == -1         # y NULL with T > 0
+    # the FFN's alignment rules are checked before the routing is enqueued
+    assert lay(fake + 8, fake, 16, fake, fake, big) == -7     # x not 16-byte aligned
+    assert lay(fake, fake, 16, fake + 8, fake, big) == -7     # y not 16-byte aligned
     r.E = 16
     assert lay(fake, fake, 16, fake, fake, big) == -2         # expert counts differ
+    # the layer from hidden states checks everything before the router is enqueued
+    P16 = L.Q4PackedC(fake, 16, 256, 128, 0)
+    lr = lambda x, y, ws: lib.moe_layer_router(x, fake, 16, ctypes.byref(P16), fake,
+                                               ctypes.byref(r), y, ws, big, None)
+    assert lr(fake, fake, fake + 8) == -7                     # workspace not 16-byte aligned
+    assert lr(fake, fake + 8, fake) == -7                     # y not 16-byte aligned
+    assert lr(None, fake, fake) == -1                         # x NULL with T > 0
