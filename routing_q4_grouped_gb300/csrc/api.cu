@@ -383,14 +383,14 @@ moe_status noalloc_scratch(void** out) {
 
 std::mutex g_ev_mu;
 cudaEvent_t g_events[8] = {};
-int g_nevents = 0;
+std::atomic<int> g_nevents{0};
 
 }  // namespace
 
 void stage_mark(int i, cudaStream_t s) {
-  if (g_nevents == 0) return;   // the common case: no timing requested
+  if (g_nevents.load(std::memory_order_relaxed) == 0) return;   // the common case: no timing requested
   std::lock_guard<std::mutex> g(g_ev_mu);
-  if (i < g_nevents && g_events[i]) cudaEventRecord(g_events[i], s);
+  if (i < g_nevents.load(std::memory_order_relaxed) && g_events[i]) cudaEventRecord(g_events[i], s);
 }
 
 }  // namespace moeq4
@@ -552,7 +552,7 @@ moe_status moe_debug_set_stage_events(void* const* events, int32_t n) {
   if (n < 0 || n > 8 || (n > 0 && !events)) return MOE_ERR_ARG;
   std::lock_guard<std::mutex> g(g_ev_mu);
   for (int i = 0; i < 8; ++i) g_events[i] = (i < n) ? static_cast<cudaEvent_t>(events[i]) : nullptr;
-  g_nevents = n;
+  g_nevents.store(n);
   return MOE_OK;
 }
 
