@@ -120,6 +120,15 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _need(fn, t, dtype, name, optional=False):
+    """The library reads every array as a dense row-major device buffer."""
+    if t is None and optional:
+        return
+    if t is None or not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        got = "None" if t is None else f"{t.dtype} on {t.device}, contiguous={t.is_contiguous()}"
+        raise ValueError(f"{fn}: {name} must be a contiguous {dtype} CUDA tensor, got {got}")
+
+
 def _stream(stream) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -240,7 +249,7 @@ class RouteBuffers:
 
 
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    """Zero-filled scratch (the routing part must start zeroed)."""
+    """Zero-filled scratch (the FFN part's grid-barrier counter must start at zero)."""
     return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
@@ -248,7 +257,7 @@ def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 def moe_route(logits: torch.Tensor, out: RouteBuffers, ws: torch.Tensor, stream=None) -> None:
     """Routing of fp32 logits [T, E] into ``out`` (asynchronous)."""
-    assert logits.dtype == torch.float32 and logits.is_contiguous()
+    _need("moe_route", logits, torch.float32, "logits")
     c = out.cstruct()
     _check("moe_route", lib().moe_route(_ptr(logits), ctypes.byref(c), _ptr(ws), ws.numel(),
                                         _stream(stream)))
@@ -260,7 +269,7 @@ def moe_route_noalloc(logits: torch.Tensor, out: RouteBuffers, stream=None) -> N
     For callers that cannot allocate device memory; limited to T <= 8192,
     E <= 256, k <= 8. Calls that overlap on the GPU share the scratch and race.
     """
-    assert logits.dtype == torch.float32 and logits.is_contiguous()
+    _need("moe_route_noalloc", logits, torch.float32, "logits")
     c = out.cstruct()
     _check("moe_route_noalloc", lib().moe_route_noalloc(_ptr(logits), ctypes.byref(c), _stream(stream)))
 
@@ -268,8 +277,8 @@ def moe_route_noalloc(logits: torch.Tensor, out: RouteBuffers, stream=None) -> N
 def moe_expert_ffn(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.Tensor,
                    ws: torch.Tensor, stream=None) -> None:
     """Grouped expert FFN: bf16 x [T, d] -> bf16 y [T, d] (asynchronous)."""
-    assert x.dtype == torch.bfloat16 and y.dtype == torch.bfloat16
-    assert x.is_contiguous() and y.is_contiguous()
+    _need("moe_expert_ffn", x, torch.bfloat16, "x")
+    _need("moe_expert_ffn", y, torch.bfloat16, "y")
     T, d = x.shape
     wc, rc = W.cstruct(), r.cstruct()
     _check("moe_expert_ffn", lib().moe_expert_ffn(_ptr(x), T, d, ctypes.byref(wc), ctypes.byref(rc),
@@ -279,8 +288,8 @@ def moe_expert_ffn(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.
 def moe_expert_ffn_decode(x: torch.Tensor, W: DeviceWeights, r: RouteBuffers, y: torch.Tensor,
                           ws: torch.Tensor, stream=None) -> None:
     """The small-batch expert FFN (T <= 64): split-K weight streaming on the CUDA cores."""
-    assert x.dtype == torch.bfloat16 and y.dtype == torch.bfloat16
-    assert x.is_contiguous() and y.is_contiguous()
+    _need("moe_expert_ffn_decode", x, torch.bfloat16, "x")
+    _need("moe_expert_ffn_decode", y, torch.bfloat16, "y")
     T, d = x.shape
     wc, rc = W.cstruct(), r.cstruct()
     _check("moe_expert_ffn_decode",
@@ -296,7 +305,9 @@ def moe_debug_set_decode_max_t(t: int) -> None:
 def moe_layer(x: torch.Tensor, logits: torch.Tensor, W: DeviceWeights, r: RouteBuffers,
               y: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
     """Routing then expert FFN on one stream, no host synchronisation."""
-    assert x.dtype == torch.bfloat16 and logits.dtype == torch.float32
+    _need("moe_layer", x, torch.bfloat16, "x")
+    _need("moe_layer", logits, torch.float32, "logits")
+    _need("moe_layer", y, torch.bfloat16, "y")
     T = x.shape[0]
     wc, rc = W.cstruct(), r.cstruct()
     _check("moe_layer", lib().moe_layer(_ptr(x), _ptr(logits), T, ctypes.byref(wc), ctypes.byref(rc),
@@ -307,8 +318,9 @@ def moe_router_topk(x: torch.Tensor, w_router: torch.Tensor, out: RouteBuffers,
                     logits: torch.Tensor = None, stream=None) -> None:
     """Router projection x [T, d] . w_router [E, d]^T with the top-k fused:
     writes out.ids / out.w (and logits [T, E] fp32 when given)."""
-    assert x.dtype == torch.bfloat16 and w_router.dtype == torch.bfloat16
-    assert x.is_contiguous() and w_router.is_contiguous()
+    _need("moe_router_topk", x, torch.bfloat16, "x")
+    _need("moe_router_topk", w_router, torch.bfloat16, "w_router")
+    _need("moe_router_topk", logits, torch.float32, "logits", optional=True)
     T, d = x.shape
     rc = out.cstruct()
     _check("moe_router_topk", lib().moe_router_topk(_ptr(x), _ptr(w_router), T, d, _ptr(logits),
@@ -326,7 +338,10 @@ def moe_layer_router(x: torch.Tensor, w_router: torch.Tensor, W: DeviceWeights, 
                      y: torch.Tensor, ws: torch.Tensor, logits: torch.Tensor = None,
                      stream=None) -> None:
     """The layer from hidden states: fused router, routing from its choice, expert FFN."""
-    assert x.dtype == torch.bfloat16 and w_router.dtype == torch.bfloat16
+    _need("moe_layer_router", x, torch.bfloat16, "x")
+    _need("moe_layer_router", w_router, torch.bfloat16, "w_router")
+    _need("moe_layer_router", y, torch.bfloat16, "y")
+    _need("moe_layer_router", logits, torch.float32, "logits", optional=True)
     T = x.shape[0]
     wc, rc = W.cstruct(), r.cstruct()
     _check("moe_layer_router", lib().moe_layer_router(_ptr(x), _ptr(w_router), T, ctypes.byref(wc),
@@ -336,6 +351,8 @@ def moe_layer_router(x: torch.Tensor, w_router: torch.Tensor, W: DeviceWeights, 
 
 def moe_residual_rms(y: torch.Tensor, x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
     """Next layer's input of the chunked run: bf16((y + x) / rms(y + x)) per token."""
+    for name, t in (("y", y), ("x", x), ("out", out)):
+        _need("moe_residual_rms", t, torch.bfloat16, name)
     T, d = x.shape
     _check("moe_residual_rms", lib().moe_residual_rms(_ptr(y), _ptr(x), _ptr(out), T, d,
                                                       _stream(stream)))

@@ -167,3 +167,23 @@ def test_ffn_and_layer_arguments_rejected_on_host(L):
     assert lr(fake, fake, fake + 8) == -7                     # workspace not 16-byte aligned
     assert lr(fake, fake + 8, fake) == -7                     # y not 16-byte aligned
     assert lr(None, fake, fake) == -1                         # x NULL with T > 0
+
+
+def test_binding_rejects_host_or_strided_tensors_before_the_library():
+    # the binding hands raw pointers to the library, which reads dense row-major
+    # device arrays: anything else is refused in Python, before any call
+    import torch
+    from routing_q4_grouped_gb300 import moeq4
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    lg = torch.zeros((4, 8), dtype=torch.float32)
+    with pytest.raises(ValueError, match="moe_layer: x must be a contiguous torch.bfloat16 CUDA"):
+        moeq4.moe_layer(x, lg, None, None, x, None)
+    with pytest.raises(ValueError, match="moe_route: logits must be .* torch.float32"):
+        moeq4.moe_route(lg.double(), None, None)
+    with pytest.raises(ValueError, match="moe_router_topk: x must be"):
+        moeq4.moe_router_topk(x, None, None)
+    with pytest.raises(ValueError, match="moe_residual_rms: y must be"):
+        moeq4.moe_residual_rms(x, x.t(), x)
+    assert not moeq4._need("f", None, torch.float32, "logits", optional=True)
+    with pytest.raises(ValueError, match="got None"):
+        moeq4._need("f", None, torch.float32, "logits")
