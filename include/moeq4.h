@@ -52,9 +52,11 @@ typedef int32_t moe_status;
 #define MOE_DEVERR_SCAN_TIMEOUT     2  /* reserved (routing has no waits; never set) */
 #define MOE_DEVERR_PIPE_TIMEOUT     4  /* a GEMM pipeline or grid barrier wait gave up */
 #define MOE_DEVERR_BAD_TILE         8  /* a block-map entry was out of range */
-#define MOE_DEVERR_BAD_WORKSPACE   16  /* routing or FFN scratch counters were not zero at
-                                          launch, or a row could not be placed (its write
-                                          was skipped) */
+#define MOE_DEVERR_BAD_WORKSPACE   16  /* the FFN scratch counters were not zero at launch,
+                                          or the routing's count rows did not add up to
+                                          T*k (a scratch shared by overlapping calls) and
+                                          a row could not be placed (its write was
+                                          skipped) */
 
 /* One 4-bit groupwise-affine matrix [R][K] ([A] §5-1; [C] glossary):
  *   qw    uint32 [R][K/8]   8 codes per word, code c of a row in word c/8 at bits 4*(c%8)
