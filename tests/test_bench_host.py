@@ -53,3 +53,17 @@ def test_device_weight_recipe_on_the_host():
     nib = torch.stack([(q >> (4 * i)) & 15 for i in range(8)]).flatten()
     assert nib.min() == 0 and nib.max() == 15
     assert abs(nib.float().mean().item() - 7.5) < 0.1  # uniform codes
+
+
+def test_launch_count_follows_the_routing_block_rule():
+    # routing is one launch while one block (kRouteTokensMin tokens at least)
+    # covers the batch, two otherwise; the FFN adds two launches, or three on
+    # the small-batch path
+    import re
+    src = open(os.path.join(ROOT, "routing_q4_grouped_gb300", "csrc", "internal.h")).read()
+    tmin = int(re.search(r"kRouteTokensMin\s*=\s*(\d+)", src).group(1))
+    assert bench.launches_per_layer(1) == 1 + 2
+    assert bench.launches_per_layer(tmin) == 1 + 2
+    assert bench.launches_per_layer(tmin + 1) == 2 + 2
+    assert bench.launches_per_layer(4096) == 4
+    assert bench.launches_per_layer(1, decode=True) == 1 + 3
